@@ -1,0 +1,472 @@
+"""Benchmark of the GLM-5.3 MTP draft head on GB300: one JSON line.
+
+Workload (the GLM-scale BF16 drafting chain): H=6144, V=154880, B=1, eps=1e-6, synthetic weights
+drawn on the GPU (embed / lm_head / eh_proj ~ N(0, 0.02), norm weights ~ 1 + N(0, 0.1)), target
+hidden states ~ N(0, 1) from seeds 1..1000, first token from seed 1; each step drafts one token
+and feeds it (device-resident) into the next step. A step = the whole hot path: the fused input
+stage (embedding gather, enorm, hnorm, concat, eh_proj) and the fused output stage (final norm,
+lm_head sweep, argmax) -- 2.05 GB of weights streamed per step, 16x the L2, so every step reads
+HBM. The timed steps are one CUDA-graph replay of the K-step chain.
+
+Reported: value = algorithmic HBM bytes per step / time per step (GB/s, all ranks), the sweep
+kernel's roofline (a timed loop of back-to-back sweeps), the same for the FP8 E4M3 head, an
+end-to-end figure through the host-buffer C entry point (host->device inputs and the draft back
+each step), SM clocks sampled during the timed loops, and the CPU oracle on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "lm_head draft sweep µs and HBM GB/s (BF16/FP8, H=6144, V=154880, B=1)"
+H, V, B = 6144, 154880, 1
+EPS = synth.EPS
+CHAIN = 1000
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sweep_traffic.json")
+SWEEP_SOURCES = [os.path.join(ROOT, "mtp_speculative_draft_head_gb300", "csrc", f)
+                 for f in ("sweep.cu", "common.cuh", "internal.h")]
+
+
+# ------------------------------------------------------------------ algorithmic bytes
+def sweep_bytes(w_bytes: int, b: int = B, logits: bool = False) -> int:
+    """lm_head (+ FP8 row scales) read once, x and final_norm_w read, draft (+ logits) written."""
+    n = V * H * w_bytes + (V * 4 if w_bytes == 1 else 0) + b * H * 2 + H * 2 + b * 4
+    return n + (b * V * 4 if logits else 0)
+
+
+def input_bytes(b: int = B) -> int:
+    """eh_proj read once, the embedding rows, target_hidden, two norm weights, x written, tokens."""
+    return H * 2 * H * 2 + b * H * 2 + b * H * 2 + 2 * H * 2 + b * H * 2 + b * 4
+
+
+def step_bytes(w_bytes: int) -> int:
+    return input_bytes() + sweep_bytes(w_bytes)
+
+
+# ------------------------------------------------------------------ distributed helpers
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (timing only; no data-path collective)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(local_ms: float, bytes_per_step: int, steps: int, world: int) -> dict:
+    """Whole-job figures: every rank runs its own replica; time = the slowest rank."""
+    ms = max_over_ranks(local_ms, world)
+    total = bytes_per_step * steps * world
+    return {"ms": ms, "ms_per_step": ms / steps, "gbs": total / (ms * 1e-3) / 1e9}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not getattr(self, "out", ""):
+            return None
+        rows = [r for r in csv.reader(io.StringIO(self.out)) if len(r) >= 10]
+        if not rows:
+            return None
+
+        def num(s):
+            try:
+                return float(s.strip())
+            except ValueError:
+                return None
+
+        loaded = [r for r in rows if (num(r[4]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in loaded if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i in range(4) if r[6 + i].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max((num(r[3]) or 0) for r in rows)}
+
+
+# ------------------------------------------------------------------ helpers
+def peak_hbm():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def sweep_source_sha() -> str:
+    h = hashlib.sha256()
+    for p in SWEEP_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, only if the sweep sources have not
+    changed since it was captured."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = t.get(kernel)
+    if not entry or entry.get("source_sha") != sweep_source_sha():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def timed_graph(graph, stream, reps: int = 1) -> float:
+    """ms for `reps` replays of a captured graph, CUDA events on the launching stream."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def capture(fn):
+    import mtp_speculative_draft_head_gb300 as m
+    return m.MtpDraftHead.capture(fn)
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, world, rank, local):
+    import mtp_speculative_draft_head_gb300 as m
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    K, W = args.steps, args.warmup
+    w = synth.make_weights(H, V, 0, dev)
+    head = m.MtpDraftHead(w.embed, w.lm_head, w.eh_proj, w.enorm_w, w.hnorm_w, w.final_norm_w, eps=EPS,
+                          max_batch=16)
+    if head.quantize_fp8() != 0:
+        raise RuntimeError("FP8 quantisation failed")
+    n_hidden = min(CHAIN, max(K, W))
+    hiddens = torch.cat([synth.chain_hidden(H, i + 1, dev) for i in range(n_hidden)]).view(n_hidden, 1, H)
+    first = synth.chain_first_token(V, dev)
+    stream = torch.cuda.Stream(dev)
+    tok = torch.empty((max(K, W) + 1, 1), dtype=torch.int32, device=dev)
+    x = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def chain_fn(n, fp8):
+        Wt, s, wt = head._head(fp8)
+
+        def fn(st):
+            for i in range(n):
+                m.mtp_head_forward_batched(head.embed, head.enorm_w, head.hnorm_w, head.eh_proj,
+                                           head.final_norm_w, Wt, s, wt, tok[i], hiddens[i % n_hidden], x,
+                                           None, tok[i + 1], head.ws, status, EPS, st)
+        return fn
+
+    def sweep_fn(n, fp8):
+        Wt, s, wt = head._head(fp8)
+        d = torch.empty(1, dtype=torch.int32, device=dev)
+
+        def fn(st):
+            for _ in range(n):
+                m.mtp_head_logits_argmax_batched(x, head.final_norm_w, Wt, s, wt, None, d, head.ws, status,
+                                                 EPS, st)
+        return fn
+
+    def input_fn(n):
+        def fn(st):
+            for i in range(n):
+                m.mtp_head_input_batched(head.embed, head.enorm_w, head.hnorm_w, head.eh_proj, tok[i % K],
+                                         hiddens[i % n_hidden], x, status, EPS, st)
+        return fn
+
+    results = {}
+    tok[0].copy_(first)
+    with torch.cuda.stream(stream):
+        # warm-up: W eager steps of each kind
+        for fp8 in (False, True):
+            chain_fn(W, fp8)(stream)
+            sweep_fn(W, fp8)(stream)
+        input_fn(W)(stream)
+    torch.cuda.synchronize()
+    graphs = {("chain", False): capture(chain_fn(K, False)), ("chain", True): capture(chain_fn(K, True)),
+              ("sweep", False): capture(sweep_fn(K, False)), ("sweep", True): capture(sweep_fn(K, True)),
+              ("input", None): capture(input_fn(K))}
+    torch.cuda.synchronize()
+    for g in graphs.values():  # one untimed replay each
+        g.replay()
+    torch.cuda.synchronize()
+    launches_all = 0
+    with ClockSampler(local) as clocks:
+        for key in (("chain", False), ("chain", True), ("sweep", False), ("sweep", True), ("input", None)):
+            barrier(world)
+            ms = timed_graph(graphs[key], torch.cuda.current_stream())
+            barrier(world)
+            results[key] = ms
+            launches_all += 2 * K if key[0] == "chain" else K
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}: {m.strerror(int(status.item()))}")
+    drafts = tok[1:K + 1].view(-1)
+    if not bool(((drafts >= 0) & (drafts < V)).all()):
+        raise RuntimeError("a draft fell outside [0, V)")
+
+    bf = aggregate(results[("chain", False)], step_bytes(2), K, world)
+    f8 = aggregate(results[("chain", True)], step_bytes(1), K, world)
+    sw_bf = aggregate(results[("sweep", False)], sweep_bytes(2), K, world)
+    sw_f8 = aggregate(results[("sweep", True)], sweep_bytes(1), K, world)
+    inp = aggregate(results[("input", None)], input_bytes(), K, world)
+
+    # end to end through the host-buffer entry point: inputs copied in and the draft copied out
+    # every step, synchronous like the source's forward_one
+    ke = min(K, 200)
+    hid_host = hiddens[:n_hidden].cpu().pin_memory()
+    th = torch.empty(1, dtype=torch.int32).pin_memory()
+    dh = torch.empty(1, dtype=torch.int32).pin_memory()
+    td = torch.empty(1, dtype=torch.int32, device=dev)
+    hd = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
+    xd = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
+    dd = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def e2e_steps(n):
+        th[0] = int(first.item())
+        for i in range(n):
+            m.mtp_head_forward_host(head.embed, head.enorm_w, head.hnorm_w, head.eh_proj, head.final_norm_w,
+                                    head.lm_head, None, m.W_BF16, th, hid_host[i % n_hidden], td, hd, xd, dd,
+                                    dh, head.ws, None, EPS, stream)
+            th[0] = dh[0]
+
+    e2e_steps(W)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    e2e_steps(ke)
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world)
+    e2e_gbs = step_bytes(2) * ke * world / (e2e_ms * 1e-3) / 1e9
+
+    peak, peak_src = peak_hbm()
+    kname = "sweep_tma_kernel<BF16,B=1>"
+    achieved = sweep_bytes(2) / (results[("sweep", False)] / K * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(bf["gbs"], 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(bf["ms_per_step"], 5),
+        "us_per_step": round(bf["ms_per_step"] * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded, drawn on the GPU; no trained weights)",
+        "impl": "ours",
+        "config": {"workload": "GLM-5.3 MTP draft chain: H=6144, V=154880, B=1, BF16 lm_head, "
+                               "device-resident token feedback, K steps in one CUDA graph",
+                   "H": H, "V": V, "B": B, "eps": EPS, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (2.06 GB of weights streamed per step, L2 129 MB)",
+                   "bytes_per_step": step_bytes(2)},
+        "stages": {"input_us": round(inp["ms_per_step"] * 1e3, 2), "input_gbs": round(inp["gbs"], 1),
+                   "sweep_bf16_us": round(sw_bf["ms_per_step"] * 1e3, 2), "sweep_bf16_gbs": round(sw_bf["gbs"], 1),
+                   "sweep_fp8_us": round(sw_f8["ms_per_step"] * 1e3, 2), "sweep_fp8_gbs": round(sw_f8["gbs"], 1)},
+        "fp8": {"us_per_step": round(f8["ms_per_step"] * 1e3, 2), "value": round(f8["gbs"], 1),
+                "unit": "GB/s", "bytes_per_step": step_bytes(1),
+                "sweep_roofline_frac": round(sweep_bytes(1) / (results[("sweep", True)] / K * 1e-3) / 1e9 / peak, 4)},
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kname),
+                     "bytes_per_launch": sweep_bytes(2), "peak_source": peak_src,
+                     "timing": "K back-to-back launches in one CUDA graph, CUDA events on the launching stream"},
+        "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "us_per_step": round(e2e_ms / ke * 1e3, 2),
+                "h2d_bytes_per_step": 4 + H * 2, "d2h_bytes_per_step": 4, "steps": ke,
+                "api": "mtp_head_forward_host (pinned host buffers, synchronous per step)"},
+        "gpu_launches": 2 * K,  # the BF16 chain region `value` is timed on: 2 kernels per step
+        "gpu_launches_all_timed_regions": launches_all,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, hiddens, first, seconds=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ CPU oracle
+SAMPLE_DIV = 64  # one sample = 1/64 of a draft step's rows (both GEMVs), norms in full
+
+
+def _oracle_sample_setup(w, hiddens, first, n_slices: int):
+    """Host copies of what the samples touch: eh_proj, the needed lm_head slices, norms."""
+    wb = {k: synth.bits(getattr(w, k)) for k in ("enorm_w", "hnorm_w", "final_norm_w", "eh_proj")}
+    tok = int(first.item())
+    wb["embed_row"] = synth.bits(w.embed[tok])
+    rows = V // SAMPLE_DIV
+    slices = []
+    for j in range(n_slices):
+        v0 = (j * 7919 % SAMPLE_DIV) * rows
+        slices.append((v0, synth.bits(w.lm_head[v0:v0 + rows])))
+    return wb, slices, [synth.bits(hiddens[i % hiddens.shape[0]]) for i in range(n_slices)]
+
+
+def oracle_sample_step(wb, lm_slice, hidden_bits, j):
+    """1/64 of one draft step on the oracle: enorm, hnorm and the final norm in full, 1/64 of the
+    eh_proj rows and 1/64 of the vocabulary; returns the algorithmic bytes it covered."""
+    import oracle
+    c = np.concatenate([oracle.rms_norm(wb["embed_row"], wb["enorm_w"], EPS),
+                        oracle.rms_norm(hidden_bits.reshape(-1), wb["hnorm_w"], EPS)])
+    r = H // SAMPLE_DIV
+    n0 = (j * 13 % SAMPLE_DIV) * r
+    xs = oracle.f64_to_bf16(oracle.logits(0, wb["eh_proj"], None, c, n0, n0 + r))
+    x = np.zeros(H, np.uint16)
+    x[n0:n0 + r] = xs
+    xhat = oracle.final_norm(x, wb["final_norm_w"], EPS)
+    lg = oracle.logits(0, lm_slice, None, xhat)
+    oracle.argmax(lg)
+    return step_bytes(2) / SAMPLE_DIV
+
+
+def cpu_baseline(w, hiddens, first, seconds: float = 12.0) -> dict:
+    import oracle
+    oracle.build()
+    n_slices = 8
+    wb, slices, hb = _oracle_sample_setup(w, hiddens, first, n_slices)
+    t0 = time.perf_counter()
+    done, nbytes, j = 0, 0.0, 0
+    while True:
+        v0, sl = slices[j % n_slices]
+        nbytes += oracle_sample_step(wb, sl, hb[j % n_slices], j)
+        done += 1
+        j += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} samples of 1/{SAMPLE_DIV} of a draft step each (eh_proj and lm_head row "
+                      f"slices, norms in full), fp64 C oracle, one thread, {dt:.1f} s",
+            "us_per_step_equiv": round(dt / done * SAMPLE_DIV * 1e6, 1)}
+
+
+def run_reference(args, world, rank):
+    """The oracle timed as it stands on the host cores: each step is a 1/64 sample of a draft step."""
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = synth.make_weights(H, V, 0, dev)
+    hiddens = torch.cat([synth.chain_hidden(H, i + 1, dev) for i in range(8)]).view(8, 1, H)
+    first = synth.chain_first_token(V, dev)
+    n_slices = 8
+    wb, slices, hb = _oracle_sample_setup(w, hiddens, first, n_slices)
+    del w
+    for j in range(args.warmup):
+        oracle_sample_step(wb, slices[j % n_slices][1], hb[j % n_slices], j)
+    t0 = time.perf_counter()
+    nbytes = 0.0
+    for j in range(args.steps):
+        nbytes += oracle_sample_step(wb, slices[j % n_slices][1], hb[j % n_slices], j)
+    dt = time.perf_counter() - t0
+    gbs = nbytes / dt / 1e9
+    sample = (f"each step = 1/{SAMPLE_DIV} of a draft step (eh_proj and lm_head row slices, norms in full), "
+              f"fp64 C oracle, one thread")
+    line = {"metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "impl": "reference",
+            "config": {"workload": "GLM-5.3 MTP draft chain: H=6144, V=154880, B=1, BF16 lm_head "
+                                   f"(1/{SAMPLE_DIV} row sample per step)", "H": H, "V": V, "B": B},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+/*
+ * mtp_head.h -- C ABI of libmtphead.so, the GB300 (sm_103a) hot path of the GLM-5.3 MTP
+ * speculative draft head (the `Glm5NextMtpHead::forward_one` draft step).
+ *
+ * What it computes, for each of B independent sequences b (the decoder layer between the two
+ * stages is the identity here; the source pages: "metrale_model_arch / glm5next_mtp_head.rs",
+ * module doc math summary and `forward_one`):
+ *
+ *   input stage   c_b    = [ enorm(embed[token_b, :]) | hnorm(target_hidden_b) ]   [2H] BF16
+ *                 x_b    = bf16( eh_proj . c_b )                                     [H]  BF16
+ *   output stage  xhat_b = shared_head.norm(x_b)                                     [H]  BF16
+ *                 logit_b[v] = lm_head[v, :] . xhat_b   (BF16 head, or the FP8 E4M3 copy
+ *                              with per-row scale: s[v] * sum_k e4m3(Q[v, k]) * xhat_b[k])
+ *                 draft_b = lowest v with logit_b[v] == max_u logit_b[u]
+ *
+ *   norm(x; w) = rms_norm_vanilla = bf16( x * w / sqrt(mean(x^2) + eps) )  -- never 1 + w
+ *   ("metrale_model_arch / glm5next_layer / mod.rs", module doc invariant).
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless the argument says "host". The caller owns every
+ *     buffer (weights, activations, outputs, workspace); the library allocates nothing and
+ *     keeps no state beyond cached device attributes.
+ *   - BF16 values are passed as uint16_t bit patterns, FP8 E4M3 codes as uint8_t (OCP E4M3
+ *     "fn": bias 7, subnormals, max 448, no infinities). All matrices are row-major and dense.
+ *   - Base pointers of matrices and vectors must be 16-byte aligned (every cudaMalloc /
+ *     PyTorch allocation is); int32/float pointers 4-byte aligned. Misalignment returns
+ *     MTP_ERR_ALIGN before anything is launched.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and the
+ *     call returns without waiting, except mtp_head_forward_host, which is synchronous.
+ *   - The return value reports host-checkable errors (arguments, shapes, alignment,
+ *     workspace size) and launch failures (MTP_ERR_CUDA). Nothing is launched when it is not
+ *     MTP_OK. Data-dependent errors (a token outside [0, V), a NaN/Inf weight handed to the
+ *     quantiser, a kernel-side wait that gave up) are written by the kernels to the optional
+ *     device word `status`: the first error stored wins; the caller zeroes it and reads it
+ *     after synchronising. The library never clears it.
+ *   - Shapes: 1 <= B <= 16, 1 <= H <= 65536, 1 <= V < 2^31, eps finite and >= 0.
+ *   - Programmatic dependent launch: the input stage and the output stage are launched so that
+ *     they may start streaming their weight matrix (eh_proj / lm_head) before the previous
+ *     kernel on the stream has finished. They read tokens, target_hidden, x, the norm weights
+ *     and the workspace only after it has finished. Do not write those two weight matrices in
+ *     a kernel that itself triggers early launch of its dependents.
+ */
+#ifndef MTP_HEAD_H
+#define MTP_HEAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MTP_OK = 0,
+    MTP_ERR_ARG = -1,             /* null pointer, bad enum, eps not finite or negative */
+    MTP_ERR_SHAPE = -2,           /* B, H or V outside the supported range */
+    MTP_ERR_ALIGN = -3,           /* a pointer is not aligned as stated above */
+    MTP_ERR_WORKSPACE = -4,       /* workspace NULL or smaller than mtp_head_workspace_bytes */
+    MTP_ERR_CUDA = -5,            /* a CUDA runtime call or launch failed */
+    MTP_ERR_NONFINITE = -6,       /* (device status) the quantiser met a NaN or Inf weight */
+    MTP_ERR_TOKEN_RANGE = -7,     /* (device status) a token outside [0, V) */
+    MTP_ERR_NOT_IMPLEMENTED = -8, /* shape combination without a kernel in this build */
+    MTP_ERR_TIMEOUT = -9          /* (device status) a kernel-side wait ran out of time */
+} mtp_status;
+
+enum { MTP_W_BF16 = 0, MTP_W_FP8_E4M3 = 1 };
+
+/* ------------------------------------------------------------------------------------------
+ * Input stage ("glm5next_mtp_head.rs", `forward_one`: the embedding row read by pointer at
+ * token*hidden, `norm` with enorm into concat[0:H] and hnorm into concat[H:2H], then the
+ * `eh_proj` dense gemv with n = H, k = 2H). One fused kernel per call.
+ *
+ *   embed          [V, H]  BF16   token embedding table (row token_b is gathered)
+ *   enorm_w        [H]     BF16   enorm weight
+ *   hnorm_w        [H]     BF16   hnorm weight
+ *   eh_proj        [H, 2H] BF16   projection; row n is output n, columns [0:H) meet the enorm
+ *                                 half of the concat, [H:2H) the hnorm half
+ *   tokens         [B]     int32  device-resident tokens (a graph replay or a draft chain
+ *                                 can feed the previous draft straight back in)
+ *   target_hidden  [B, H]  BF16   the target model's hidden state for each sequence
+ *   x_out          [B, H]  BF16   output: the block input x
+ *   status         [1]     int32  optional (may be NULL); MTP_ERR_TOKEN_RANGE if some token is
+ *                                 outside [0, V): that sequence's x row is written as zeros and
+ *                                 the embedding table is not read for it
+ * ---------------------------------------------------------------------------------------- */
+int mtp_head_input_batched(const uint16_t* embed, const uint16_t* enorm_w,
+                           const uint16_t* hnorm_w, const uint16_t* eh_proj,
+                           const int32_t* tokens, const uint16_t* target_hidden,
+                           uint16_t* x_out, int32_t* status, int B, int H, int V, float eps,
+                           void* stream);
+
+/* Same, B = 1. */
+int mtp_head_input(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hnorm_w,
+                   const uint16_t* eh_proj, const int32_t* token, const uint16_t* target_hidden,
+                   uint16_t* x_out, int32_t* status, int H, int V, float eps, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Output stage ("glm5next_mtp_head.rs", `forward_one`: `shared_head.norm` in place, then the
+ * `lm_head` dense gemv -- or `dense_gemv_fp8w` over the FP8 copy described in the `head_fp8`
+ * doc -- then `argmax_bf16`; here the sweep covers the whole vocabulary on one GPU and the
+ * argmax is fused into it). One kernel per call; lm_head is read once for all B sequences.
+ *
+ *   x              [B, H]  BF16   block output
+ *   final_norm_w   [H]     BF16   shared_head.norm weight
+ *   lm_head        [V, H]  BF16 (w_dtype MTP_W_BF16) or E4M3 codes (MTP_W_FP8_E4M3)
+ *   row_scale      [V]     fp32   per-row scale of the FP8 copy; NULL for BF16
+ *   logits         [B, V]  fp32   optional output (NULL = not stored). Kept in fp32, not BF16.
+ *   draft          [B]     int32  output: lowest index of the maximum logit; NaN never wins;
+ *                                 -1 if every logit of that sequence is NaN
+ *   status         [1]     int32  optional (may be NULL); MTP_ERR_TIMEOUT on a kernel-side wait
+ *   workspace             device scratch of at least mtp_head_workspace_bytes(B, H, V)
+ *                         bytes, zero-filled once before its first use. The kernel returns it
+ *                         to zero itself, so it stays valid across calls and CUDA-graph
+ *                         replays. Two calls that may run at the same time (different streams)
+ *                         need different workspaces.
+ * ---------------------------------------------------------------------------------------- */
+int mtp_head_logits_argmax_batched(const uint16_t* x, const uint16_t* final_norm_w,
+                                   const void* lm_head, const float* row_scale, int w_dtype,
+                                   float* logits, int32_t* draft, int32_t* status,
+                                   void* workspace, size_t workspace_bytes, int B, int H, int V,
+                                   float eps, void* stream);
+
+/* Same, B = 1. */
+int mtp_head_logits_argmax(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_head,
+                           const float* row_scale, int w_dtype, float* logits, int32_t* draft,
+                           int32_t* status, void* workspace, size_t workspace_bytes, int H,
+                           int V, float eps, void* stream);
+
+/* Bytes of workspace the output stage needs (no device query; 0 for invalid shapes). */
+size_t mtp_head_workspace_bytes(int B, int H, int V);
+
+/* ------------------------------------------------------------------------------------------
+ * Whole draft step, device buffers: the input stage into x, then the output stage from x.
+ * Exactly mtp_head_input_batched followed by mtp_head_logits_argmax_batched on one stream.
+ * ---------------------------------------------------------------------------------------- */
+int mtp_head_forward_batched(const uint16_t* embed, const uint16_t* enorm_w,
+                             const uint16_t* hnorm_w, const uint16_t* eh_proj,
+                             const uint16_t* final_norm_w, const void* lm_head,
+                             const float* row_scale, int w_dtype, const int32_t* tokens,
+                             const uint16_t* target_hidden, uint16_t* x, float* logits,
+                             int32_t* draft, int32_t* status, void* workspace,
+                             size_t workspace_bytes, int B, int H, int V, float eps,
+                             void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Whole draft step from HOST buffers, synchronous: the shape of the source's
+ * `forward_one(token, hidden_in, ...) -> u32`, which synchronises and copies the draft to the
+ * host. Copies tokens_host [B] and hidden_host [B, H] into the caller's device buffers
+ * tokens_dev / hidden_dev, runs mtp_head_forward_batched, copies draft back into
+ * draft_host [B] and waits for the stream. Host buffers should be pinned for asynchronous
+ * copies. The device `status` word, if given, is read back too and returned when nonzero.
+ * ---------------------------------------------------------------------------------------- */
+int mtp_head_forward_host(const uint16_t* embed, const uint16_t* enorm_w,
+                          const uint16_t* hnorm_w, const uint16_t* eh_proj,
+                          const uint16_t* final_norm_w, const void* lm_head,
+                          const float* row_scale, int w_dtype,
+                          const int32_t* tokens_host, const uint16_t* hidden_host,
+                          int32_t* tokens_dev, uint16_t* hidden_dev, uint16_t* x_dev,
+                          int32_t* draft_dev, int32_t* draft_host, int32_t* status,
+                          void* workspace, size_t workspace_bytes, int B, int H, int V,
+                          float eps, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * FP8 E4M3 copy of a [V, H] BF16 matrix ("glm5next_mtp_head.rs", `head_fp8` doc: an E4M3
+ * copy of lm_head used for drafting only). Per row v:
+ *   row_scale[v] = fp32( max_k |w[v, k]| / 448 )
+ *   q[v, k]      = e4m3_rne_satfinite( fp32( w[v, k] / row_scale[v] ) )
+ * An all-zero row gives scale 0 and zero codes. A NaN or Inf weight stores
+ * MTP_ERR_NONFINITE in `status` (required here) and that row's codes and scale as zeros; the
+ * copy must then not be used (the source's "quantisation fails" case).
+ *   w [V, H] BF16 -> q [V, H] uint8 (E4M3 codes), row_scale [V] fp32
+ * ---------------------------------------------------------------------------------------- */
+int mtp_head_quantize_fp8(const uint16_t* w, uint8_t* q, float* row_scale, int32_t* status,
+                          int V, int H, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* mtp_head_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MTP_HEAD_H */

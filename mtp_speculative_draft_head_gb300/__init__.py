@@ -1,0 +1,16 @@
+"""GB300 (sm_103a) hot path of the GLM-5.3 MTP speculative draft head.
+
+The computation lives in ``libmtphead.so`` (CUDA, C ABI declared in ``include/mtp_head.h``):
+the fused input stage (embedding gather, enorm/hnorm RMSNorm, concat, eh_proj GEMV), the fused
+output stage (shared_head.norm, lm_head vocabulary sweep in BF16 or FP8 E4M3, argmax) and the
+FP8 quantiser. ``_lib`` binds those entry points by name with ctypes; ``MtpDraftHead`` owns
+buffers around them. PyTorch provides device memory and streams only.
+"""
+from ._lib import (  # noqa: F401
+    ERR_ALIGN, ERR_ARG, ERR_CUDA, ERR_NONFINITE, ERR_NOT_IMPLEMENTED, ERR_SHAPE, ERR_TIMEOUT,
+    ERR_TOKEN_RANGE, ERR_WORKSPACE, OK, W_BF16, W_FP8_E4M3, MTPError, SIGNATURES, load,
+    mtp_head_forward_batched, mtp_head_forward_host, mtp_head_input, mtp_head_input_batched,
+    mtp_head_logits_argmax, mtp_head_logits_argmax_batched, mtp_head_quantize_fp8,
+    mtp_head_workspace_bytes, strerror, workspace,
+)
+from .head import MtpDraftHead  # noqa: F401

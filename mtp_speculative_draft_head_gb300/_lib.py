@@ -1,0 +1,205 @@
+"""ctypes binding of libmtphead.so (include/mtp_head.h): argument marshalling only.
+
+Each function has the name of the C entry point it calls and takes torch tensors where the C
+function takes device (or host) pointers: the binding passes ``tensor.data_ptr()``, the
+current CUDA stream (or the one given) and the sizes, and raises ``MTPError`` when the C call
+returns a nonzero status. Every step of the computation runs in the library's CUDA kernels;
+there is no fallback. If the shared library cannot be built or loaded, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+W_BF16 = 0
+W_FP8_E4M3 = 1
+
+OK = 0
+ERR_ARG = -1
+ERR_SHAPE = -2
+ERR_ALIGN = -3
+ERR_WORKSPACE = -4
+ERR_CUDA = -5
+ERR_NONFINITE = -6
+ERR_TOKEN_RANGE = -7
+ERR_NOT_IMPLEMENTED = -8
+ERR_TIMEOUT = -9
+
+# name -> (restype, argtypes); mirrors include/mtp_head.h
+P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "mtp_head_input_batched": (I, [P, P, P, P, P, P, P, P, I, I, I, F, P]),
+    "mtp_head_input": (I, [P, P, P, P, P, P, P, P, I, I, F, P]),
+    "mtp_head_logits_argmax_batched": (I, [P, P, P, P, I, P, P, P, P, Z, I, I, I, F, P]),
+    "mtp_head_logits_argmax": (I, [P, P, P, P, I, P, P, P, P, Z, I, I, F, P]),
+    "mtp_head_workspace_bytes": (Z, [I, I, I]),
+    "mtp_head_forward_batched": (I, [P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, Z, I, I, I, F, P]),
+    "mtp_head_forward_host": (I, [P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, P, P, Z, I, I, I, F, P]),
+    "mtp_head_quantize_fp8": (I, [P, P, P, P, I, I, P]),
+    "mtp_head_strerror": (ctypes.c_char_p, [I]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class MTPError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: status {code}: {strerror(code)}")
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load (building first if needed) libmtphead.so and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        lib_path = path or _build.build()
+        if not os.path.exists(lib_path):
+            raise RuntimeError(f"libmtphead.so not found at {lib_path}")
+        lib = ctypes.CDLL(lib_path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def strerror(code: int) -> str:
+    return load().mtp_head_strerror(int(code)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _dev(t, name):
+    if t is not None and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return _ptr(t)
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(code: int, where: str) -> int:
+    if code != OK:
+        raise MTPError(code, where)
+    return code
+
+
+def mtp_head_workspace_bytes(B: int, H: int, V: int) -> int:
+    return int(load().mtp_head_workspace_bytes(B, H, V))
+
+
+def workspace(B: int, H: int, V: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace tensor for the output stage (reusable across calls)."""
+    n = mtp_head_workspace_bytes(B, H, V)
+    if n == 0:
+        raise MTPError(ERR_SHAPE, "workspace")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def mtp_head_input_batched(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidden, x_out,
+                           status=None, eps: float = 1e-6, stream=None) -> None:
+    V, H = embed.shape
+    B = tokens.numel()
+    _check(load().mtp_head_input_batched(
+        _dev(embed, "embed"), _dev(enorm_w, "enorm_w"), _dev(hnorm_w, "hnorm_w"),
+        _dev(eh_proj, "eh_proj"), _dev(tokens, "tokens"), _dev(target_hidden, "target_hidden"),
+        _dev(x_out, "x_out"), _dev(status, "status"), B, H, V, eps, _stream(stream)),
+        "mtp_head_input_batched")
+
+
+def mtp_head_input(embed, enorm_w, hnorm_w, eh_proj, token, target_hidden, x_out, status=None,
+                   eps: float = 1e-6, stream=None) -> None:
+    V, H = embed.shape
+    _check(load().mtp_head_input(
+        _dev(embed, "embed"), _dev(enorm_w, "enorm_w"), _dev(hnorm_w, "hnorm_w"),
+        _dev(eh_proj, "eh_proj"), _dev(token, "token"), _dev(target_hidden, "target_hidden"),
+        _dev(x_out, "x_out"), _dev(status, "status"), H, V, eps, _stream(stream)),
+        "mtp_head_input")
+
+
+def mtp_head_logits_argmax_batched(x, final_norm_w, lm_head, row_scale, w_dtype: int, logits,
+                                   draft, ws, status=None, eps: float = 1e-6, stream=None) -> None:
+    V, H = lm_head.shape
+    B = draft.numel()
+    _check(load().mtp_head_logits_argmax_batched(
+        _dev(x, "x"), _dev(final_norm_w, "final_norm_w"), _dev(lm_head, "lm_head"),
+        _dev(row_scale, "row_scale"), int(w_dtype), _dev(logits, "logits"), _dev(draft, "draft"),
+        _dev(status, "status"), _dev(ws, "workspace"), ws.numel() * ws.element_size(), B, H, V,
+        eps, _stream(stream)),
+        "mtp_head_logits_argmax_batched")
+
+
+def mtp_head_logits_argmax(x, final_norm_w, lm_head, row_scale, w_dtype: int, logits, draft, ws,
+                           status=None, eps: float = 1e-6, stream=None) -> None:
+    V, H = lm_head.shape
+    _check(load().mtp_head_logits_argmax(
+        _dev(x, "x"), _dev(final_norm_w, "final_norm_w"), _dev(lm_head, "lm_head"),
+        _dev(row_scale, "row_scale"), int(w_dtype), _dev(logits, "logits"), _dev(draft, "draft"),
+        _dev(status, "status"), _dev(ws, "workspace"), ws.numel() * ws.element_size(), H, V, eps,
+        _stream(stream)),
+        "mtp_head_logits_argmax")
+
+
+def mtp_head_forward_batched(embed, enorm_w, hnorm_w, eh_proj, final_norm_w, lm_head, row_scale,
+                             w_dtype: int, tokens, target_hidden, x, logits, draft, ws,
+                             status=None, eps: float = 1e-6, stream=None) -> None:
+    V, H = embed.shape
+    B = tokens.numel()
+    _check(load().mtp_head_forward_batched(
+        _dev(embed, "embed"), _dev(enorm_w, "enorm_w"), _dev(hnorm_w, "hnorm_w"),
+        _dev(eh_proj, "eh_proj"), _dev(final_norm_w, "final_norm_w"), _dev(lm_head, "lm_head"),
+        _dev(row_scale, "row_scale"), int(w_dtype), _dev(tokens, "tokens"),
+        _dev(target_hidden, "target_hidden"), _dev(x, "x"), _dev(logits, "logits"),
+        _dev(draft, "draft"), _dev(status, "status"), _dev(ws, "workspace"),
+        ws.numel() * ws.element_size(), B, H, V, eps, _stream(stream)),
+        "mtp_head_forward_batched")
+
+
+def mtp_head_forward_host(embed, enorm_w, hnorm_w, eh_proj, final_norm_w, lm_head, row_scale,
+                          w_dtype: int, tokens_host, hidden_host, tokens_dev, hidden_dev, x_dev,
+                          draft_dev, draft_host, ws, status=None, eps: float = 1e-6,
+                          stream=None) -> None:
+    """Synchronous draft step from host buffers (tokens_host, hidden_host, draft_host are CPU
+    tensors, pinned for asynchronous copies)."""
+    V, H = embed.shape
+    B = tokens_host.numel()
+    for t, n in ((tokens_host, "tokens_host"), (hidden_host, "hidden_host"), (draft_host, "draft_host")):
+        if t.is_cuda:
+            raise ValueError(f"{n} must be a host tensor")
+    _check(load().mtp_head_forward_host(
+        _dev(embed, "embed"), _dev(enorm_w, "enorm_w"), _dev(hnorm_w, "hnorm_w"),
+        _dev(eh_proj, "eh_proj"), _dev(final_norm_w, "final_norm_w"), _dev(lm_head, "lm_head"),
+        _dev(row_scale, "row_scale"), int(w_dtype), _ptr(tokens_host), _ptr(hidden_host),
+        _dev(tokens_dev, "tokens_dev"), _dev(hidden_dev, "hidden_dev"), _dev(x_dev, "x_dev"),
+        _dev(draft_dev, "draft_dev"), _ptr(draft_host), _dev(status, "status"),
+        _dev(ws, "workspace"), ws.numel() * ws.element_size(), B, H, V, eps, _stream(stream)),
+        "mtp_head_forward_host")
+
+
+def mtp_head_quantize_fp8(w, q, row_scale, status, stream=None) -> None:
+    V, H = w.shape
+    _check(load().mtp_head_quantize_fp8(
+        _dev(w, "w"), _dev(q, "q"), _dev(row_scale, "row_scale"), _dev(status, "status"), V, H,
+        _stream(stream)),
+        "mtp_head_quantize_fp8")

@@ -1,0 +1,244 @@
+// Input stage of the MTP draft head, one fused kernel ("glm5next_mtp_head.rs", `forward_one`:
+// the embedding row read by pointer at token*hidden, `norm` with enorm into concat[0:H] and
+// with hnorm into concat[H:2H], then the `eh_proj` dense gemv, n = H, k = 2H).
+//
+// Design: the same persistent, per-warp TMA-pipelined row stream as the output stage, here over
+// the [H, 2H] eh_proj rows. The gather is an address computation on the device-resident token
+// (so a draft chain or a CUDA graph can feed the previous draft straight back in), and every
+// CTA builds the normalised concat for its B sequences in shared memory while its first weight
+// stages are already in flight.
+//
+// Accuracy: x is rounded to BF16 right after this sum, so the sum is error-free up to the final
+// rounding: every product of two BF16 values is exact in fp32, and each one is added to a
+// per-lane double-float (hi, lo) with TwoSum (four independent accumulators per lane, element
+// e going to e % 4); accumulators and lanes are combined the same way and the value is rounded
+// once to BF16. x therefore equals the BF16 rounding of the exact sum unless that sum lies
+// within ~2^-40 relative of a rounding midpoint.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mtp {
+
+namespace {
+
+__device__ __forceinline__ bool token_ok(int32_t tok, int V) { return tok >= 0 && tok < V; }
+
+// Build c_b = [enorm(embed[tok_b]) | hnorm(hidden_b)] for all sequences into shared memory.
+template <int NB_MAX>
+__device__ void build_concat(const InputArgs& a, int nb, uint16_t* vec, int vec_elems, float* red,
+                             bool* valid) {
+  const int H = a.H;
+  for (int b = 0; b < nb; ++b) {
+    const int32_t tok = a.tokens[b];
+    const bool ok = token_ok(tok, a.V);
+    valid[b] = ok;
+    if (!ok && threadIdx.x == 0) store_status(a.status, MTP_ERR_TOKEN_RANGE);
+    uint16_t* cb = vec + static_cast<size_t>(b) * vec_elems;
+    const uint16_t* erow = ok ? a.embed + static_cast<int64_t>(tok) * H : a.embed;
+    rms_norm_to_smem<kThreads>(erow, a.enorm_w, H, a.eps, cb, red, ok, LayoutIdentity{});
+    __syncthreads();
+    rms_norm_to_smem<kThreads>(a.hidden + static_cast<size_t>(b) * H, a.hnorm_w, H, a.eps, cb + H,
+                               red, true, LayoutIdentity{});
+    __syncthreads();
+  }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads, 1) input_tma_kernel(const InputArgs a) {
+  constexpr int NW = kWarps;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ bool valid_s[kMaxB];
+
+  const int S = a.stages;
+  const int H = a.H;
+  const int K = 2 * H;
+  const int64_t row_bytes = static_cast<int64_t>(K) * 2;
+  const int cpr = static_cast<int>((row_bytes + kChunk - 1) / kChunk);
+  const uint32_t last_bytes = static_cast<uint32_t>(row_bytes - static_cast<int64_t>(cpr - 1) * kChunk);
+  const int vec_elems = ((K / 8 + 31) / 32) * 32 * 8;
+
+  uint8_t* stages = smem;
+  uint16_t* vec = reinterpret_cast<uint16_t*>(stages + static_cast<size_t>(NW) * S * kChunk);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(vec + static_cast<size_t>(NB) * vec_elems);
+  float* red = reinterpret_cast<float*>(bars + NW * S);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r0 = static_cast<int64_t>(H) * blockIdx.x / gridDim.x;
+  const int64_t r1 = static_cast<int64_t>(H) * (blockIdx.x + 1) / gridDim.x;
+  const int64_t cta_rows = r1 - r0;
+  const int nrows = cta_rows > warp ? static_cast<int>((cta_rows - warp + NW - 1) / NW) : 0;
+  const int nitems = nrows * cpr;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NW * S; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  uint8_t* my_stages = stages + static_cast<size_t>(warp) * S * kChunk;
+  uint64_t* my_bars = bars + warp * S;
+  const uint64_t policy = l2_evict_first_policy();
+  const uint8_t* W = reinterpret_cast<const uint8_t*>(a.eh_proj);
+  int pi = 0, pc = 0, ps = 0;
+  auto issue_next = [&]() {
+    const int64_t row = r0 + warp + static_cast<int64_t>(pi) * NW;
+    const uint32_t bytes = (pc == cpr - 1) ? last_bytes : static_cast<uint32_t>(kChunk);
+    const uint8_t* src = W + row * row_bytes + static_cast<int64_t>(pc) * kChunk;
+    const uint32_t bar = smem_addr(&my_bars[ps]);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_copy_g2s(smem_addr(my_stages + static_cast<size_t>(ps) * kChunk), src, bytes, bar, policy);
+    if (++pc == cpr) { pc = 0; ++pi; }
+    if (++ps == S) ps = 0;
+  };
+  const int prefill = nitems < S ? nitems : S;
+  if (lane == 0)
+    for (int t = 0; t < prefill; ++t) issue_next();
+
+  // tokens and target_hidden may come from the preceding kernel
+  pdl_wait_prior_grid();
+  build_concat<NB>(a, NB, vec, vec_elems, red, valid_s);
+  bool valid[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) valid[b] = valid_s[b];
+  pdl_launch_dependents();
+
+  DF acc[NB][4];
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[b][e] = DF{0.0f, 0.0f};
+  int ci = 0, cc = 0, cs = 0, t_fail = -1;
+  uint32_t parity = 0;
+  for (int t = 0; t < nitems; ++t) {
+    const uint32_t bar = smem_addr(&my_bars[cs]);
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar, parity))) {
+      t_fail = t;
+      break;
+    }
+    const uint4* wv = reinterpret_cast<const uint4*>(my_stages + static_cast<size_t>(cs) * kChunk);
+    const int nv = static_cast<int>(((cc == cpr - 1) ? last_bytes : static_cast<uint32_t>(kChunk)) >> 4);
+    const int J0 = cc * (kChunk / 16);
+#pragma unroll 2
+    for (int j = lane; j < nv; j += 32) {
+      const uint4 q = wv[j];
+      const float wf[8] = {bf16_lo(q.x), bf16_hi(q.x), bf16_lo(q.y), bf16_hi(q.y),
+                           bf16_lo(q.z), bf16_hi(q.z), bf16_lo(q.w), bf16_hi(q.w)};
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const uint4 cq = reinterpret_cast<const uint4*>(vec + static_cast<size_t>(b) * vec_elems)[J0 + j];
+        const float cf[8] = {bf16_lo(cq.x), bf16_hi(cq.x), bf16_lo(cq.y), bf16_hi(cq.y),
+                             bf16_lo(cq.z), bf16_hi(cq.z), bf16_lo(cq.w), bf16_hi(cq.w)};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) df_add(acc[b][e & 3], __fmul_rn(wf[e], cf[e]));  // exact product
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && t + S < nitems) {
+      fence_proxy_async_smem();
+      issue_next();
+    }
+    if (++cs == S) { cs = 0; parity ^= 1u; }
+    if (++cc == cpr) {
+      const int64_t row = r0 + warp + static_cast<int64_t>(ci) * NW;
+      cc = 0;
+      ++ci;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        DF v = df_add(df_add(acc[b][0], acc[b][1]), df_add(acc[b][2], acc[b][3]));
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) v = df_add(v, shfl_xor_df(v, m));
+        if (lane == 0) a.x[static_cast<size_t>(b) * H + row] = valid[b] ? bf16_rne_df(v.hi, v.lo) : uint16_t(0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[b][e] = DF{0.0f, 0.0f};
+      }
+    }
+  }
+  if (t_fail >= 0 && lane == 0) {
+    store_status(a.status, MTP_ERR_TIMEOUT);
+    int s = cs;
+    uint32_t par = parity;
+    for (int u = t_fail; u < nitems && u < t_fail + S; ++u) {
+      (void)mbar_wait_bounded(smem_addr(&my_bars[s]), par);
+      if (++s == S) { s = 0; par ^= 1u; }
+    }
+  }
+}
+
+// Plain-load input stage for any H and B <= 16: one warp per output row.
+__global__ void __launch_bounds__(kThreads) input_plain_kernel(const InputArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ bool valid_s[kMaxB];
+  const int H = a.H, K = 2 * H, nb = a.B;
+  const int vec_elems = ((K + 7) / 8) * 8;
+  uint16_t* vec = reinterpret_cast<uint16_t*>(smem);
+  float* red = reinterpret_cast<float*>(vec + static_cast<size_t>(nb) * vec_elems);
+
+  pdl_wait_prior_grid();
+  build_concat<kMaxB>(a, nb, vec, vec_elems, red, valid_s);
+  pdl_launch_dependents();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  const int64_t tw = static_cast<int64_t>(gridDim.x) * kWarps;
+  for (int64_t row = gw; row < H; row += tw) {
+    const uint16_t* wr = a.eh_proj + row * K;
+    for (int b = 0; b < nb; ++b) {
+      const uint16_t* cb = vec + static_cast<size_t>(b) * vec_elems;
+      DF acc{0.0f, 0.0f};
+      for (int k = lane; k < K; k += 32)
+        df_add(acc, __fmul_rn(bf16_bits_to_f32(wr[k]), bf16_bits_to_f32(cb[k])));
+      for (int m = 16; m > 0; m >>= 1) acc = df_add(acc, shfl_xor_df(acc, m));
+      if (lane == 0) a.x[static_cast<size_t>(b) * H + row] = valid_s[b] ? bf16_rne_df(acc.hi, acc.lo) : uint16_t(0);
+    }
+  }
+}
+
+cudaError_t launch_input_kernel(void (*kernel)(InputArgs), unsigned grid, size_t smem,
+                                cudaStream_t stream, InputArgs a) {
+  void* args[] = {&a};
+  return launch_pdl(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(kThreads), smem, stream, args);
+}
+
+}  // namespace
+
+cudaError_t launch_input_stage(const InputArgs& in, cudaStream_t stream) {
+  DeviceInfo di;
+  cudaError_t err = device_info(&di);
+  if (err != cudaSuccess) return err;
+  InputArgs a = in;
+  const int K = 2 * a.H;
+  const int64_t want = (static_cast<int64_t>(a.H) + kWarps - 1) / kWarps;
+  int64_t grid = di.sm_count < want ? di.sm_count : want;
+  if (grid < 1) grid = 1;
+  const size_t misc = static_cast<size_t>(2 * kWarps + 2) * sizeof(float) + 256;
+  const bool rows16 = (K % 8) == 0;
+  if (rows16 && a.B <= kTmaMaxB) {
+    const int vec_elems = ((K / 8 + 31) / 32) * 32 * 8;
+    const size_t fixed = static_cast<size_t>(a.B) * vec_elems * 2 + misc;
+    const size_t per_stage = static_cast<size_t>(kWarps) * (kChunk + 8);
+    if (fixed + 2 * per_stage <= static_cast<size_t>(di.smem_optin)) {
+      int S = static_cast<int>((static_cast<size_t>(di.smem_optin) - fixed) / per_stage);
+      if (S > kMaxStages) S = kMaxStages;
+      a.stages = S;
+      const size_t smem = fixed + static_cast<size_t>(S) * per_stage;
+      void (*k)(InputArgs) = nullptr;
+      switch (a.B) {
+        case 1: k = input_tma_kernel<1>; break;
+        case 2: k = input_tma_kernel<2>; break;
+        case 3: k = input_tma_kernel<3>; break;
+        default: k = input_tma_kernel<4>; break;
+      }
+      return launch_input_kernel(k, static_cast<unsigned>(grid), smem, stream, a);
+    }
+  }
+  const int vec_elems = ((K + 7) / 8) * 8;
+  const size_t smem = static_cast<size_t>(a.B) * vec_elems * 2 + misc;
+  if (smem > static_cast<size_t>(di.smem_optin)) return cudaErrorNotSupported;
+  a.stages = 0;
+  return launch_input_kernel(input_plain_kernel, static_cast<unsigned>(grid), smem, stream, a);
+}
+
+}  // namespace mtp

@@ -1,0 +1,83 @@
+// Host-side declarations shared by the translation units of libmtphead.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mtp {
+
+// Tuning constants of the streaming kernels (compile-time; see the kernels for their use).
+#ifndef MTP_WARPS
+#define MTP_WARPS 8
+#endif
+#ifndef MTP_CHUNK
+#define MTP_CHUNK 4096
+#endif
+#ifndef MTP_MAX_STAGES
+#define MTP_MAX_STAGES 6
+#endif
+#ifndef MTP_MIXED_FMA
+#define MTP_MIXED_FMA 0
+#endif
+
+constexpr int kWarps = MTP_WARPS;
+constexpr int kThreads = kWarps * 32;
+constexpr int kChunk = MTP_CHUNK;        // bytes per pipeline stage
+constexpr int kMaxStages = MTP_MAX_STAGES;
+constexpr int kTmaMaxB = 4;              // the CUDA-core streaming kernels take B <= 4
+
+constexpr int kSmemReserve = 1024;      // opt-in bytes kept back for static shared variables
+
+struct DeviceInfo {
+  int sm_count;
+  int smem_optin;  // dynamic shared memory a block may use (opt-in maximum - kSmemReserve)
+};
+
+// Cached per device; returns cudaSuccess or the error of the first query.
+cudaError_t device_info(DeviceInfo* info);
+
+// cudaLaunchKernelExC with programmatic stream serialization allowed; raises the kernel's
+// dynamic shared memory limit once per device. device_info() must have been called first.
+cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       void** args);
+
+struct InputArgs {
+  const uint16_t* embed;
+  const uint16_t* enorm_w;
+  const uint16_t* hnorm_w;
+  const uint16_t* eh_proj;
+  const int32_t* tokens;
+  const uint16_t* hidden;
+  uint16_t* x;
+  int32_t* status;
+  int B, H, V;
+  float eps;
+  int stages;
+};
+
+struct SweepArgs {
+  const uint16_t* x;
+  const uint16_t* final_norm_w;
+  const uint8_t* W;      // lm_head bytes (BF16 pairs or E4M3 codes)
+  const float* scale;    // FP8 row scales or nullptr
+  float* logits;         // may be nullptr
+  int32_t* draft;
+  int32_t* status;
+  uint8_t* ws;
+  int w_dtype;
+  int B, H, V;
+  float eps;
+  int stages;
+};
+
+cudaError_t launch_input_stage(const InputArgs& a, cudaStream_t stream);
+cudaError_t launch_sweep(const SweepArgs& a, cudaStream_t stream);
+cudaError_t launch_quantize(const uint16_t* w, uint8_t* q, float* scale, int32_t* status,
+                            int V, int H, cudaStream_t stream);
+
+// Workspace layout of the output stage: a 128-byte header (the CTA completion counter), then
+// one (value, index) partial per CTA and sequence.
+size_t sweep_workspace_bytes(int B);
+
+}  // namespace mtp

@@ -1,0 +1,130 @@
+"""``MtpDraftHead``: the GLM-5.3 MTP draft head on one GPU, as a thin owner of buffers around
+the C ABI (include/mtp_head.h).
+
+It mirrors the source's `Glm5NextMtpHead` ("metrale_model_arch / glm5next_mtp_head.rs"): the
+weights it holds are ``embed_tokens``, ``eh_proj``, ``enorm``, ``hnorm``, ``final_norm`` and the
+target's ``lm_head`` (plus the optional FP8 copy of the `head_fp8` doc); its per-sequence scratch
+is the ``x`` / ``logits`` / ``draft`` buffers of the proposer state. The decoder layer between
+the two stages is the identity here. Every computation is a call into libmtphead.so.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import W_BF16, W_FP8_E4M3
+
+
+class MtpDraftHead:
+    def __init__(self, embed, lm_head, eh_proj, enorm_w, hnorm_w, final_norm_w, eps: float = 1e-6,
+                 max_batch: int = 16):
+        for name, t in (("embed", embed), ("lm_head", lm_head), ("eh_proj", eh_proj),
+                        ("enorm_w", enorm_w), ("hnorm_w", hnorm_w), ("final_norm_w", final_norm_w)):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+        self.embed, self.lm_head, self.eh_proj = embed, lm_head, eh_proj
+        self.enorm_w, self.hnorm_w, self.final_norm_w = enorm_w, hnorm_w, final_norm_w
+        self.V, self.H = embed.shape
+        if lm_head.shape != (self.V, self.H) or eh_proj.shape != (self.H, 2 * self.H):
+            raise ValueError("shapes: embed/lm_head [V, H], eh_proj [H, 2H]")
+        self.eps = float(eps)
+        self.device = embed.device
+        self.max_batch = max_batch
+        self.lm_head_fp8 = None
+        self.row_scale = None
+        self.ws = _lib.workspace(max_batch, self.H, self.V, self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    # ------------------------------------------------------------------ FP8 copy
+    def quantize_fp8(self) -> int:
+        """Build the E4M3 copy of lm_head with per-row FP32 scales; returns the device status
+        (0, or MTP_ERR_NONFINITE when a weight is NaN/Inf -- the copy is then dropped)."""
+        q = torch.empty((self.V, self.H), dtype=torch.uint8, device=self.device)
+        s = torch.empty(self.V, dtype=torch.float32, device=self.device)
+        st = torch.zeros(1, dtype=torch.int32, device=self.device)
+        _lib.mtp_head_quantize_fp8(self.lm_head, q, s, st)
+        code = int(st.item())
+        if code == 0:
+            self.lm_head_fp8, self.row_scale = q, s
+        else:
+            self.lm_head_fp8, self.row_scale = None, None
+        return code
+
+    def _head(self, fp8: bool):
+        if fp8:
+            if self.lm_head_fp8 is None:
+                raise RuntimeError("no FP8 copy: call quantize_fp8() first")
+            return self.lm_head_fp8, self.row_scale, W_FP8_E4M3
+        return self.lm_head, None, W_BF16
+
+    # ------------------------------------------------------------------ stages
+    def input(self, tokens, hidden, x=None, status=None, stream=None):
+        B = tokens.numel()
+        x = torch.empty((B, self.H), dtype=torch.bfloat16, device=self.device) if x is None else x
+        _lib.mtp_head_input_batched(self.embed, self.enorm_w, self.hnorm_w, self.eh_proj, tokens,
+                                    hidden, x, status, self.eps, stream)
+        return x
+
+    def logits_argmax(self, x, fp8: bool = False, logits=True, draft=None, status=None, stream=None):
+        B = x.shape[0]
+        W, s, wt = self._head(fp8)
+        if logits is True:
+            logits = torch.empty((B, self.V), dtype=torch.float32, device=self.device)
+        elif logits is False:
+            logits = None
+        draft = torch.empty(B, dtype=torch.int32, device=self.device) if draft is None else draft
+        _lib.mtp_head_logits_argmax_batched(x, self.final_norm_w, W, s, wt, logits, draft, self.ws,
+                                            status, self.eps, stream)
+        return logits, draft
+
+    def forward(self, tokens, hidden, fp8: bool = False, logits=False, x=None, draft=None,
+                status=None, stream=None):
+        """One draft step for B sequences (device buffers): returns (x, logits|None, draft)."""
+        B = tokens.numel()
+        W, s, wt = self._head(fp8)
+        x = torch.empty((B, self.H), dtype=torch.bfloat16, device=self.device) if x is None else x
+        if logits is True:
+            logits = torch.empty((B, self.V), dtype=torch.float32, device=self.device)
+        elif logits is False:
+            logits = None
+        draft = torch.empty(B, dtype=torch.int32, device=self.device) if draft is None else draft
+        _lib.mtp_head_forward_batched(self.embed, self.enorm_w, self.hnorm_w, self.eh_proj,
+                                      self.final_norm_w, W, s, wt, tokens, hidden, x, logits, draft,
+                                      self.ws, status, self.eps, stream)
+        return x, logits, draft
+
+    # ------------------------------------------------------------------ draft chains
+    def chain(self, first_tokens, hiddens, fp8: bool = False, graph: bool = True, status=None):
+        """Draft ``steps`` tokens per sequence, each step feeding its draft (device-resident) into
+        the next step's input stage: hiddens is [steps, B, H]; returns drafts [steps, B] int32.
+        With ``graph`` the whole chain is captured once in a CUDA graph and replayed."""
+        steps, B, _ = hiddens.shape
+        tok = torch.empty((steps + 1, B), dtype=torch.int32, device=self.device)
+        tok[0].copy_(first_tokens.view(-1))
+        x = torch.empty((B, self.H), dtype=torch.bfloat16, device=self.device)
+        W, s, wt = self._head(fp8)
+
+        def run(stream=None):
+            for i in range(steps):
+                _lib.mtp_head_forward_batched(self.embed, self.enorm_w, self.hnorm_w, self.eh_proj,
+                                              self.final_norm_w, W, s, wt, tok[i], hiddens[i], x,
+                                              None, tok[i + 1], self.ws, status, self.eps, stream)
+
+        if not graph:
+            run()
+            return tok[1:]
+        g = self.capture(run)
+        g.replay()
+        return tok[1:]
+
+    @staticmethod
+    def capture(fn) -> torch.cuda.CUDAGraph:
+        """Capture fn(stream) into a CUDA graph on a side stream (warming the launch path first)."""
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                fn(s)
+        torch.cuda.current_stream().wait_stream(s)
+        return g

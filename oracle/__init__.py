@@ -59,7 +59,7 @@ def _load():
         lib.mo_e4m3_to_f64_array.argtypes = [P, P, I64]
         lib.mo_f64_to_e4m3_array.argtypes = [P, P, I64]
         lib.mo_rms_norm.argtypes = [P, P, I64, ctypes.c_double, P]
-        lib.mo_input_stage.argtypes = [P, P, P, P, I64, P, I64, I64, ctypes.c_double, P, P, P]
+        lib.mo_input_stage.argtypes = [P, P, P, P, I64, P, I64, I64, ctypes.c_double, P, P, P, P]
         lib.mo_input_stage.restype = ctypes.c_int
         lib.mo_logits.argtypes = [ctypes.c_int, P, P, P, I64, I64, I64, P]
         lib.mo_logits_rows.argtypes = [ctypes.c_int, P, P, P, I64, P, I64, P]
@@ -128,10 +128,11 @@ def rms_norm(x, w, eps: float) -> np.ndarray:
 
 
 def input_stage(embed, enorm_w, hnorm_w, eh_proj, tokens, hidden, eps: float,
-                return_concat: bool = False):
+                return_concat: bool = False, return_sums: bool = False):
     """x[b] = eh_proj( concat( enorm(embed[tokens[b]]), hnorm(hidden[b]) ) ), BF16.
 
-    Returns (x [B, H] uint16, status [B] int) or (x, concat [B, 2H], status).
+    Returns (x [B, H] uint16, status [B] int); with return_concat the concat [B, 2H] comes
+    second; with return_sums the fp64 sums before rounding [B, H] come last.
     """
     embed = _c(embed, np.uint16)
     V, H = embed.shape
@@ -144,15 +145,15 @@ def input_stage(embed, enorm_w, hnorm_w, eh_proj, tokens, hidden, eps: float,
     x = np.empty((B, H), np.uint16)
     concat = np.empty((B, 2 * H), np.uint16)
     scratch = np.empty(2 * H, np.uint16)
+    sums = np.empty((B, H), np.float64)
     status = np.empty(B, np.int64)
     ew, hw = _c(enorm_w, np.uint16), _c(hnorm_w, np.uint16)
     for b in range(B):
         status[b] = _load().mo_input_stage(
             _p(embed), _p(ew), _p(hw), _p(eh_proj), int(tokens[b]), _p(hidden[b]), H, V,
-            float(np.float32(eps)), _p(concat[b]), _p(x[b]), _p(scratch))
-    if return_concat:
-        return x, concat, status
-    return x, status
+            float(np.float32(eps)), _p(concat[b]), _p(x[b]), _p(sums[b]), _p(scratch))
+    out = (x, concat, status) if return_concat else (x, status)
+    return out + (sums,) if return_sums else out
 
 
 def final_norm(x, final_norm_w, eps: float) -> np.ndarray:

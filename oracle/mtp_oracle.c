@@ -161,15 +161,16 @@ void mo_rms_norm(const uint16_t* x, const uint16_t* w, int64_t n, double eps, ui
 /*   e         = embed[token, :]            (row `token` of the [V, H] table)            */
 /*   concat    = [ enorm(e) | hnorm(hidden) ]   ([2H], BF16)                             */
 /*   x[n]      = bf16( sum_k eh_proj[n, k] * concat[k] ),  eh_proj is [H, 2H] row-major  */
-/* concat_out (2H) may be NULL. Returns MO_ERR_TOKEN_RANGE (and a zero x) when token is  */
-/* outside [0, V).                                                                       */
+/* concat_out (2H) and x_sum_out (H, the fp64 sums before the BF16 rounding) may be     */
+/* NULL. Returns MO_ERR_TOKEN_RANGE (and a zero x) when token is outside [0, V).         */
 /* ------------------------------------------------------------------------------------ */
 int mo_input_stage(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hnorm_w,
                    const uint16_t* eh_proj, int64_t token, const uint16_t* hidden,
                    int64_t H, int64_t V, double eps, uint16_t* concat_out, uint16_t* x_out,
-                   uint16_t* concat_scratch /* 2H */) {
+                   double* x_sum_out, uint16_t* concat_scratch /* 2H */) {
     if (token < 0 || token >= V) {
         for (int64_t n = 0; n < H; ++n) x_out[n] = 0;
+        if (x_sum_out) for (int64_t n = 0; n < H; ++n) x_sum_out[n] = 0.0;
         if (concat_out) memset(concat_out, 0, (size_t)(2 * H) * sizeof(uint16_t));
         return MO_ERR_TOKEN_RANGE;
     }
@@ -181,6 +182,7 @@ int mo_input_stage(const uint16_t* embed, const uint16_t* enorm_w, const uint16_
         const uint16_t* row = eh_proj + n * (2 * H);
         for (int64_t k = 0; k < 2 * H; ++k) acc += mo_bf16_to_f64(row[k]) * mo_bf16_to_f64(c[k]);
         x_out[n] = mo_f64_to_bf16(acc);
+        if (x_sum_out) x_sum_out[n] = acc;
     }
     if (concat_out) memcpy(concat_out, c, (size_t)(2 * H) * sizeof(uint16_t));
     return MO_OK;

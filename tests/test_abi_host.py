@@ -1,0 +1,148 @@
+"""The C ABI without a GPU: the library builds and loads, exports every function the header
+declares, the Python binding declares each with the header's arity, and host-side validation
+returns the documented status codes before anything is launched (the fake device addresses
+below are never dereferenced: every call here fails validation first)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mtp_speculative_draft_head_gb300 as m
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mtp_head.h")
+
+
+def _declarations():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    decls = {}
+    for mt in re.finditer(r"\b(mtp_head_\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        name, params = mt.group(1), mt.group(2).strip()
+        decls[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return decls
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return m.load()
+
+
+def test_header_declares_the_entry_points():
+    d = _declarations()
+    for name in ("mtp_head_input", "mtp_head_input_batched", "mtp_head_logits_argmax",
+                 "mtp_head_logits_argmax_batched", "mtp_head_quantize_fp8",
+                 "mtp_head_workspace_bytes", "mtp_head_forward_batched", "mtp_head_forward_host",
+                 "mtp_head_strerror"):
+        assert name in d
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declarations():
+        assert hasattr(lib, name), f"{name} is declared in mtp_head.h but not exported"
+
+
+def test_binding_matches_header_arity():
+    d = _declarations()
+    assert set(m.SIGNATURES) == set(d)
+    for name, (_, args) in m.SIGNATURES.items():
+        assert len(args) == d[name], name
+
+
+def test_strerror_covers_every_code(lib):
+    for code in range(0, -10, -1):
+        assert m.strerror(code) != "unknown status"
+    assert m.strerror(-99) == "unknown status"
+
+
+def test_workspace_bytes(lib):
+    assert m.mtp_head_workspace_bytes(1, 6144, 154880) > 0
+    assert m.mtp_head_workspace_bytes(16, 6144, 154880) >= 16 * 8 * 152
+    assert m.mtp_head_workspace_bytes(0, 6144, 154880) == 0
+    assert m.mtp_head_workspace_bytes(17, 6144, 154880) == 0
+    assert m.mtp_head_workspace_bytes(1, 0, 10) == 0
+
+
+A = 0x10000  # an aligned fake device address (never dereferenced)
+
+
+def _input(lib, **kw):
+    args = dict(embed=A, enorm_w=A, hnorm_w=A, eh_proj=A, tokens=A, hidden=A, x=A, status=None,
+                B=1, H=64, V=100, eps=1e-6)
+    args.update(kw)
+    return lib.mtp_head_input_batched(args["embed"], args["enorm_w"], args["hnorm_w"], args["eh_proj"],
+                                      args["tokens"], args["hidden"], args["x"], args["status"],
+                                      args["B"], args["H"], args["V"], args["eps"], None)
+
+
+def _output(lib, **kw):
+    args = dict(x=A, fw=A, W=A, scale=None, wt=m.W_BF16, logits=None, draft=A, status=None, ws=A,
+                ws_bytes=1 << 20, B=1, H=64, V=100, eps=1e-6)
+    args.update(kw)
+    return lib.mtp_head_logits_argmax_batched(args["x"], args["fw"], args["W"], args["scale"], args["wt"],
+                                              args["logits"], args["draft"], args["status"], args["ws"],
+                                              args["ws_bytes"], args["B"], args["H"], args["V"],
+                                              args["eps"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(embed=None), m.ERR_ARG),
+    (dict(tokens=None), m.ERR_ARG),
+    (dict(x=None), m.ERR_ARG),
+    (dict(eps=float("nan")), m.ERR_ARG),
+    (dict(eps=-1.0), m.ERR_ARG),
+    (dict(eps=float("inf")), m.ERR_ARG),
+    (dict(B=0), m.ERR_SHAPE),
+    (dict(B=17), m.ERR_SHAPE),
+    (dict(H=0), m.ERR_SHAPE),
+    (dict(H=65537), m.ERR_SHAPE),
+    (dict(V=0), m.ERR_SHAPE),
+    (dict(eh_proj=A + 8), m.ERR_ALIGN),
+    (dict(hidden=A + 2), m.ERR_ALIGN),
+    (dict(tokens=A + 2), m.ERR_ALIGN),
+])
+def test_input_stage_validation(lib, kw, code):
+    assert _input(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), m.ERR_ARG),
+    (dict(W=None), m.ERR_ARG),
+    (dict(draft=None), m.ERR_ARG),
+    (dict(wt=2), m.ERR_ARG),
+    (dict(wt=m.W_FP8_E4M3, scale=None), m.ERR_ARG),
+    (dict(eps=float("nan")), m.ERR_ARG),
+    (dict(B=0), m.ERR_SHAPE),
+    (dict(B=17), m.ERR_SHAPE),
+    (dict(V=-5), m.ERR_SHAPE),
+    (dict(W=A + 4), m.ERR_ALIGN),
+    (dict(draft=A + 1), m.ERR_ALIGN),
+    (dict(ws=A + 8), m.ERR_ALIGN),
+    (dict(ws=None), m.ERR_WORKSPACE),
+    (dict(ws_bytes=16), m.ERR_WORKSPACE),
+])
+def test_output_stage_validation(lib, kw, code):
+    assert _output(lib, **kw) == code
+
+
+def test_quantizer_validation(lib):
+    q = lib.mtp_head_quantize_fp8
+    assert q(None, A, A, A, 10, 16, None) == m.ERR_ARG
+    assert q(A, A, A, None, 10, 16, None) == m.ERR_ARG  # status is required here
+    assert q(A, A, A, A, 0, 16, None) == m.ERR_SHAPE
+    assert q(A + 2, A, A, A, 10, 16, None) == m.ERR_ALIGN
+
+
+def test_forward_host_validation(lib):
+    f = lib.mtp_head_forward_host
+    args = [A, A, A, A, A, A, None, m.W_BF16, A, A, A, A, A, A, A, None, A, 1 << 20, 1, 64, 100,
+            ctypes.c_float(1e-6), None]
+    bad = list(args)
+    bad[8] = None  # tokens_host
+    assert f(*bad) == m.ERR_ARG
+    bad = list(args)
+    bad[16] = None  # workspace
+    assert f(*bad) == m.ERR_WORKSPACE
+    bad = list(args)
+    bad[18] = 0  # B
+    assert f(*bad) == m.ERR_SHAPE

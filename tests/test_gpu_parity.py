@@ -1,0 +1,368 @@
+"""GPU parity of the CUDA library (through its C ABI) against the CPU oracle on small and
+medium shapes: several tiles and ragged tails, both weight dtypes, every kernel path
+(bulk-copy pipelines for 16-byte rows and B <= 4, plain-load kernels otherwise), plus the
+edge cases: out-of-range tokens, NaN/Inf, exact ties, determinism, CUDA-graph replay and the
+quantiser bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import mtp_speculative_draft_head_gb300 as m
+import oracle
+import synth
+from gpu_helpers import TOL_BF16, TOL_FP8, check_draft, check_logits_and_draft, check_x, lowest_argmax
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+EPS = synth.EPS
+
+
+def _bits(t):
+    return synth.bits(t)
+
+
+class Case:
+    def __init__(self, H, V, B, seed=0):
+        self.H, self.V, self.B = H, V, B
+        self.w = synth.make_weights(H, V, seed, "cpu")
+        self.tokens, self.hidden = synth.make_step_inputs(H, V, B, seed + 100, "cpu")
+        self.wb = {k: _bits(v) for k, v in self.w.as_dict().items()}
+        self.g = {k: v.to(DEV) for k, v in self.w.as_dict().items()}
+        self.ws = m.workspace(B, H, V, DEV)
+
+    def quantize_gpu(self):
+        q = torch.empty((self.V, self.H), dtype=torch.uint8, device=DEV)
+        s = torch.empty(self.V, dtype=torch.float32, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        m.mtp_head_quantize_fp8(self.g["lm_head"], q, s, st)
+        torch.cuda.synchronize()
+        return q, s, int(st.item())
+
+    def input_gpu(self, tokens=None, hidden=None):
+        tokens = self.tokens if tokens is None else tokens
+        hidden = self.hidden if hidden is None else hidden
+        B = tokens.numel()
+        x = torch.full((B, self.H), 7, dtype=torch.bfloat16, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        m.mtp_head_input_batched(self.g["embed"], self.g["enorm_w"], self.g["hnorm_w"], self.g["eh_proj"],
+                                 tokens.to(DEV), hidden.to(DEV), x, st, EPS)
+        torch.cuda.synchronize()
+        return x, int(st.item())
+
+    def output_gpu(self, x, W, scale, wt, want_logits=True):
+        B = x.shape[0]
+        logits = torch.full((B, self.V), float("nan"), dtype=torch.float32, device=DEV) if want_logits else None
+        draft = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        m.mtp_head_logits_argmax_batched(x, self.g["final_norm_w"], W, scale, wt, logits, draft, self.ws, st, EPS)
+        torch.cuda.synchronize()
+        return logits, draft, int(st.item())
+
+    def oracle_input(self):
+        return oracle.input_stage(self.wb["embed"], self.wb["enorm_w"], self.wb["hnorm_w"], self.wb["eh_proj"],
+                                  _bits(self.tokens).astype(np.int64), _bits(self.hidden), EPS,
+                                  return_sums=True)
+
+    def oracle_logits(self, x_bits, wt, W_bits, scale):
+        xhat = oracle.final_norm(x_bits, self.wb["final_norm_w"], EPS)
+        return oracle.logits(wt, W_bits, scale, xhat, threads=8).reshape(x_bits.shape[0], -1)
+
+
+SHAPES = [  # (H, V, B): tiles, ragged tails and every path
+    (256, 4096, 1),     # the small workload
+    (1000, 5003, 1),    # BF16 rows of 2000 B (one partial chunk); FP8 rows not 16-B -> plain path
+    (1000, 5003, 3),
+    (2056, 1031, 2),    # BF16 rows of 4112 B: a full chunk and a 16-byte tail chunk
+    (2048, 777, 4),     # FP8 rows of 2048 B on the bulk-copy path, B = 4
+    (6144, 1000, 1),    # GLM hidden size: 3 BF16 chunks, FP8 one full + one partial chunk
+    (4096, 300, 5),     # B = 5 -> plain kernels
+    (512, 2000, 16),    # B = 16 -> plain kernels
+    (100, 50, 2),       # odd H -> plain kernels
+    (8, 7, 1),
+    (64, 1, 1),         # V = 1
+]
+
+
+@pytest.mark.parametrize("H,V,B", SHAPES)
+@pytest.mark.parametrize("fp8", [False, True])
+def test_head_matches_oracle(H, V, B, fp8):
+    c = Case(H, V, B, seed=H + V + B)
+    x_ref, st_ref, sums = c.oracle_input()
+    assert np.all(st_ref == 0)
+    x_gpu, st = c.input_gpu()
+    assert st == 0
+    check_x(_bits(x_gpu), x_ref, sums)
+    if fp8:
+        q, s, qst = c.quantize_gpu()
+        assert qst == 0
+        q_ref, s_ref, _ = oracle.quantize(c.wb["lm_head"])
+        assert np.array_equal(_bits(q), q_ref)
+        assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+        W, scale, wt, tol, Wb, sb = q, s, m.W_FP8_E4M3, TOL_FP8, q_ref, s_ref
+    else:
+        W, scale, wt, tol, Wb, sb = c.g["lm_head"], None, m.W_BF16, TOL_BF16, c.wb["lm_head"], None
+    ref = c.oracle_logits(x_ref, wt, Wb, sb)
+    # output stage on the GPU's own x (the whole head) ...
+    logits, draft, st = c.output_gpu(x_gpu, W, scale, wt)
+    assert st == 0
+    err = check_logits_and_draft(logits.cpu().numpy(), draft.cpu().numpy(), ref, tol)
+    assert err < 5e-3  # the real error is fp32 rounding; the stated bar is far looser
+    # ... on the oracle's x (the output stage alone) ...
+    x_or = torch.from_numpy(x_ref.view(np.int16)).view(torch.bfloat16).to(DEV)
+    logits2, draft2, _ = c.output_gpu(x_or, W, scale, wt)
+    check_logits_and_draft(logits2.cpu().numpy(), draft2.cpu().numpy(), ref, tol)
+    # ... without storing logits (same draft) ...
+    _, draft3, _ = c.output_gpu(x_gpu, W, scale, wt, want_logits=False)
+    assert torch.equal(draft3, draft)
+    # ... and through the one-call forward (bitwise the same)
+    xf = torch.empty_like(x_gpu)
+    lf = torch.empty_like(logits)
+    df = torch.empty_like(draft)
+    m.mtp_head_forward_batched(c.g["embed"], c.g["enorm_w"], c.g["hnorm_w"], c.g["eh_proj"],
+                               c.g["final_norm_w"], W, scale, wt, c.tokens.to(DEV), c.hidden.to(DEV),
+                               xf, lf, df, c.ws, None, EPS)
+    torch.cuda.synchronize()
+    assert torch.equal(xf, x_gpu) and torch.equal(df, draft)
+    assert torch.equal(lf.view(torch.int32), logits.view(torch.int32))
+
+
+def test_worked_example_on_gpu(golden_dir):
+    import json
+    import os
+    ex = json.load(open(os.path.join(golden_dir, "worked_example_4x8.json")))
+
+    def t(v):
+        return torch.tensor(v, dtype=torch.float32).to(torch.bfloat16).to(DEV).contiguous()
+
+    g = dict(embed=t(ex["embed"]), enorm_w=t(ex["enorm_w"]), hnorm_w=t(ex["hnorm_w"]),
+             eh_proj=t(ex["eh_proj"]), final_norm_w=t(ex["final_norm_w"]), lm_head=t(ex["lm_head"]))
+    ws = m.workspace(1, 4, 8, DEV)
+    for hnorm_w, hid, want_x in ((ex["hnorm_w"], ex["target_hidden"], ex["expected_x"]),
+                                 (ex["variant_hnorm_w"], ex["variant_target_hidden"], ex["variant_expected_x"])):
+        x = torch.empty((1, 4), dtype=torch.bfloat16, device=DEV)
+        m.mtp_head_input(g["embed"], g["enorm_w"], t(hnorm_w), g["eh_proj"],
+                         torch.tensor([ex["token"]], dtype=torch.int32, device=DEV), t([hid]), x)
+        torch.cuda.synchronize()
+        assert x.float().cpu().view(-1).tolist() == want_x
+        logits = torch.empty((1, 8), dtype=torch.float32, device=DEV)
+        draft = torch.empty(1, dtype=torch.int32, device=DEV)
+        m.mtp_head_logits_argmax(x, g["final_norm_w"], g["lm_head"], None, m.W_BF16, logits, draft, ws)
+        torch.cuda.synchronize()
+        assert logits.cpu().view(-1).tolist() == ex["expected_logits"]
+        assert int(draft.item()) == ex["expected_draft"]
+    # FP8 copy: codes, then the tie survives and the lower index wins
+    q = torch.empty((8, 4), dtype=torch.uint8, device=DEV)
+    s = torch.empty(8, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.mtp_head_quantize_fp8(g["lm_head"], q, s, st)
+    m.mtp_head_logits_argmax(x, g["final_norm_w"], q, s, m.W_FP8_E4M3, logits, draft, ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert q.cpu().tolist() == ex["expected_fp8_codes"]
+    lg = logits.cpu().view(-1).double().numpy()
+    np.testing.assert_allclose(lg, ex["expected_logits"], rtol=ex["fp8_logit_rel_tol"], atol=1e-12)
+    assert lg[3] == lg[5] and int(draft.item()) == ex["expected_draft"]
+
+
+def test_out_of_range_tokens_flag_and_zero_rows():
+    c = Case(256, 4096, 3, seed=5)
+    tokens = torch.tensor([11, c.V + 3, -1], dtype=torch.int32)
+    x, st = c.input_gpu(tokens=tokens)
+    assert st == m.ERR_TOKEN_RANGE
+    assert torch.all(x[1:] == 0)
+    x_ref, _, sums = oracle.input_stage(c.wb["embed"], c.wb["enorm_w"], c.wb["hnorm_w"], c.wb["eh_proj"],
+                                        [11, c.V + 3, -1], _bits(c.hidden), EPS, return_sums=True)
+    check_x(_bits(x), x_ref, sums)
+    # a zero x gives all-zero logits: every logit ties and index 0 wins
+    logits, draft, _ = c.output_gpu(x, c.g["lm_head"], None, m.W_BF16)
+    assert torch.all(logits[1:] == 0) and draft[1:].tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_nan_input_gives_draft_minus_one(fp8):
+    c = Case(256, 1000, 2, seed=6)
+    x = torch.ones((2, 256), dtype=torch.bfloat16, device=DEV)
+    x[1, 17] = float("nan")
+    if fp8:
+        q, s, _ = c.quantize_gpu()
+        W, scale, wt = q, s, m.W_FP8_E4M3
+    else:
+        W, scale, wt = c.g["lm_head"], None, m.W_BF16
+    logits, draft, _ = c.output_gpu(x, W, scale, wt)
+    assert torch.isnan(logits[1]).all() and int(draft[1]) == -1
+    assert int(draft[0]) == lowest_argmax(logits[0].double().cpu().numpy())
+
+
+def test_infinite_logits_and_ties():
+    H, V = 64, 12
+    W = torch.zeros((V, H), dtype=torch.float32)
+    W[1, 0], W[1, 1] = float("inf"), float("-inf")   # inf - inf = NaN: never wins
+    W[3, 0] = float("inf")                            # +inf
+    W[7, 0] = float("inf")                            # +inf again: tie, 3 wins
+    W[5, 0] = float("-inf")
+    W[9, 2] = 1e30
+    Wd = W.to(torch.bfloat16).to(DEV)
+    fw = torch.ones(H, dtype=torch.bfloat16, device=DEV)
+    x = torch.ones((1, H), dtype=torch.bfloat16, device=DEV)
+    ws = m.workspace(1, H, V, DEV)
+    logits = torch.empty((1, V), dtype=torch.float32, device=DEV)
+    draft = torch.empty(1, dtype=torch.int32, device=DEV)
+    m.mtp_head_logits_argmax(x, fw, Wd, None, m.W_BF16, logits, draft, ws)
+    torch.cuda.synchronize()
+    lg = logits.cpu().view(-1)
+    assert torch.isnan(lg[1]) and lg[3] == float("inf") and lg[7] == float("inf") and lg[5] == float("-inf")
+    assert int(draft.item()) == 3
+    # all -inf: the lowest index wins
+    Wn = torch.zeros((V, H), dtype=torch.float32)
+    Wn[:, 0] = float("-inf")
+    m.mtp_head_logits_argmax(x, fw, Wn.to(torch.bfloat16).to(DEV), None, m.W_BF16, logits, draft, ws)
+    torch.cuda.synchronize()
+    assert int(draft.item()) == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_planted_ties_lowest_index_wins(fp8):
+    H, V = 2048, 20000
+    c = Case(H, V, 1, seed=9)
+    x_ref, _, _ = c.oracle_input()
+    xhat = oracle.final_norm(x_ref, c.wb["final_norm_w"], EPS)[0]
+    rows = synth.pick_rows(V, 16, seed=9)
+    sign = torch.from_numpy(oracle.bf16_to_f64(xhat))
+    W = synth.plant_rows(c.w.lm_head, rows, sign, 0.05)
+    Wd = W.to(DEV)
+    x_gpu, _ = c.input_gpu()
+    if fp8:
+        q = torch.empty((V, H), dtype=torch.uint8, device=DEV)
+        s = torch.empty(V, dtype=torch.float32, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        m.mtp_head_quantize_fp8(Wd, q, s, st)
+        logits, draft, _ = c.output_gpu(x_gpu, q, s, m.W_FP8_E4M3)
+    else:
+        logits, draft, _ = c.output_gpu(x_gpu, Wd, None, m.W_BF16)
+    lg = logits.cpu().view(-1)
+    planted = rows.tolist()
+    assert len(set(lg[planted].view(torch.int32).tolist())) == 1  # bit-identical tie
+    assert int(draft.item()) == min(planted)
+
+
+def test_repeat_calls_are_bitwise_identical_and_graph_replay_matches():
+    c = Case(2048, 30000, 2, seed=10)
+    x, _ = c.input_gpu()
+    outs = [c.output_gpu(x, c.g["lm_head"], None, m.W_BF16) for _ in range(3)]
+    for lg, dr, _ in outs[1:]:
+        assert torch.equal(lg.view(torch.int32), outs[0][0].view(torch.int32)) and torch.equal(dr, outs[0][1])
+    tokens, hidden = c.tokens.to(DEV), c.hidden.to(DEV)
+    xg = torch.empty_like(x)
+    lg = torch.empty((2, c.V), dtype=torch.float32, device=DEV)
+    dr = torch.empty(2, dtype=torch.int32, device=DEV)
+
+    def step(stream):
+        m.mtp_head_forward_batched(c.g["embed"], c.g["enorm_w"], c.g["hnorm_w"], c.g["eh_proj"],
+                                   c.g["final_norm_w"], c.g["lm_head"], None, m.W_BF16, tokens, hidden,
+                                   xg, lg, dr, c.ws, None, EPS, stream)
+
+    graph = m.MtpDraftHead.capture(step)
+    for _ in range(3):
+        lg.zero_()
+        dr.fill_(-5)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(xg, x)
+        assert torch.equal(lg.view(torch.int32), outs[0][0].view(torch.int32)) and torch.equal(dr, outs[0][1])
+
+
+def test_workspace_reused_across_batch_sizes():
+    c = Case(512, 3000, 4, seed=11)
+    x, _ = c.input_gpu()
+    ref = c.oracle_logits(_bits(x), 0, c.wb["lm_head"], None)
+    for B in (4, 1, 3, 1):
+        lg, dr, _ = c.output_gpu(x[:B].contiguous(), c.g["lm_head"], None, m.W_BF16)
+        check_logits_and_draft(lg.cpu().numpy(), dr.cpu().numpy(), ref[:B], TOL_BF16)
+
+
+def test_quantizer_exhaustive_patterns_bitexact():
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = pats[(pats & 0x7F80) != 0x7F80]
+    rng = np.random.default_rng(19)
+    rows = []
+    for top in (0x3F80, 0x0001, 0x0080, 0x2000, 0x4300, 0x7F7F, 0x0000):
+        r = rng.permutation(finite)
+        r = r[(r & 0x7FFF) <= top][:4096]
+        r = np.resize(r, 4096)
+        r[0] = top
+        rows.append(r)
+    Wb = np.stack(rows).astype(np.uint16)
+    q_ref, s_ref, st_ref = oracle.quantize(Wb)
+    assert st_ref == 0
+    for H in (4096, 4000):  # vector and plain paths
+        Wt = torch.from_numpy(Wb[:, :H].copy().view(np.int16)).view(torch.bfloat16).to(DEV)
+        q = torch.empty((Wb.shape[0], H), dtype=torch.uint8, device=DEV)
+        s = torch.empty(Wb.shape[0], dtype=torch.float32, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        m.mtp_head_quantize_fp8(Wt, q, s, st)
+        torch.cuda.synchronize()
+        qr, sr, _ = oracle.quantize(Wb[:, :H].copy())
+        assert int(st.item()) == 0
+        assert np.array_equal(s.cpu().numpy().view(np.uint32), sr.view(np.uint32))
+        assert np.array_equal(q.cpu().numpy(), qr)
+
+
+def test_quantizer_rejects_nonfinite_rows():
+    W = torch.randn((6, 64)) * 0.02
+    W[2, 5] = float("nan")
+    W[4, 0] = float("inf")
+    Wd = W.to(torch.bfloat16).to(DEV)
+    q = torch.full((6, 64), 0x55, dtype=torch.uint8, device=DEV)
+    s = torch.full((6,), 3.0, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.mtp_head_quantize_fp8(Wd, q, s, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == m.ERR_NONFINITE
+    assert float(s[2]) == 0.0 and float(s[4]) == 0.0 and torch.all(q[2] == 0) and torch.all(q[4] == 0)
+    q_ref, s_ref, _ = oracle.quantize(_bits(Wd))
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
+def test_draft_head_class_and_host_forward():
+    c = Case(256, 4096, 2, seed=12)
+    head = m.MtpDraftHead(c.g["embed"], c.g["lm_head"], c.g["eh_proj"], c.g["enorm_w"], c.g["hnorm_w"],
+                          c.g["final_norm_w"], eps=EPS, max_batch=2)
+    assert head.quantize_fp8() == 0
+    x_ref, _, _ = c.oracle_input()
+    for fp8 in (False, True):
+        _, logits, draft = head.forward(c.tokens.to(DEV), c.hidden.to(DEV), fp8=fp8, logits=True)
+        if fp8:
+            ref = c.oracle_logits(x_ref, 1, _bits(head.lm_head_fp8), head.row_scale.cpu().numpy())
+        else:
+            ref = c.oracle_logits(x_ref, 0, c.wb["lm_head"], None)
+        check_logits_and_draft(logits.cpu().numpy(), draft.cpu().numpy(), ref, TOL_FP8 if fp8 else TOL_BF16)
+        # host-buffer step: same draft
+        th = c.tokens.clone().pin_memory()
+        hh = c.hidden.clone().pin_memory()
+        dh = torch.empty(2, dtype=torch.int32).pin_memory()
+        W, s, wt = head._head(fp8)
+        m.mtp_head_forward_host(head.embed, head.enorm_w, head.hnorm_w, head.eh_proj, head.final_norm_w,
+                                W, s, wt, th, hh, torch.empty(2, dtype=torch.int32, device=DEV),
+                                torch.empty((2, 256), dtype=torch.bfloat16, device=DEV),
+                                torch.empty((2, 256), dtype=torch.bfloat16, device=DEV),
+                                torch.empty(2, dtype=torch.int32, device=DEV), dh, head.ws,
+                                torch.zeros(1, dtype=torch.int32, device=DEV), EPS)
+        assert dh.tolist() == draft.cpu().tolist()
+
+
+def test_short_chain_teacher_forced():
+    c = Case(512, 3000, 1, seed=13)
+    head = m.MtpDraftHead(c.g["embed"], c.g["lm_head"], c.g["eh_proj"], c.g["enorm_w"], c.g["hnorm_w"],
+                          c.g["final_norm_w"], eps=EPS, max_batch=1)
+    steps = 6
+    hiddens = torch.stack([synth.chain_hidden(512, i + 1, "cpu") for i in range(steps)]).to(DEV)
+    first = torch.tensor([17], dtype=torch.int32, device=DEV)
+    drafts_graph = head.chain(first, hiddens, graph=True).cpu().view(-1).tolist()
+    drafts_eager = head.chain(first, hiddens, graph=False).cpu().view(-1).tolist()
+    assert drafts_graph == drafts_eager
+    tok = 17
+    for i in range(steps):
+        out = oracle.head(c.wb, [tok], _bits(hiddens[i].cpu()), EPS)
+        check_draft(drafts_graph[i], None, out["logits"][0], TOL_BF16)
+        tok = drafts_graph[i]  # teacher-forced: the oracle follows the GPU's token
