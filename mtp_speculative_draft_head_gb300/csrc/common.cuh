@@ -4,7 +4,8 @@
 //    policy, async-proxy fence, programmatic dependent launch, global timer.
 //  * Exact-rounding numerics: TwoSum, double-float accumulation, BF16 round-to-nearest-even
 //    of a double-float value, the E4M3 bit-placement decode.
-//  * The RMSNorm prologue (rms_norm_vanilla, x * w / rms) computed into shared memory.
+//  * Packed f32x2 arithmetic and packed double-float accumulation.
+//  * The RMSNorm prologue (rms_norm_vanilla, x * w / rms) for several vectors, into shared memory.
 //  * The (max, lowest index) argmax combine.
 #pragma once
 
@@ -207,69 +208,167 @@ __device__ __forceinline__ void arg_update(ArgBest& b, float v, int32_t i) {
 }
 
 // ------------------------------------------------------------------------------------------
-// rms_norm_vanilla prologue: out = bf16( x * w / sqrt(mean(x^2) + eps) ), written into shared
-// memory at index layout(k). The sum of squares is kept as a double-float (each square of a
-// BF16 value is exact in fp32), 1/rms is formed in fp64 and split into two fp32 parts, and
-// x*w (exact in fp32) times 1/rms is rounded once to BF16 from a double-float -- so the result
-// is the correctly rounded BF16 of the fp64 expression up to ~2^-44 relative.
-// All NT threads of the block must call it; `red` is >= 2 * NT / 32 + 2 floats of shared memory.
-// `valid` false writes zeros without reading x.
+// Packed fp32 pairs (sm_100+ f32x2 instructions): two IEEE round-to-nearest operations per
+// instruction, lane-wise identical to the scalar ones.
 // ------------------------------------------------------------------------------------------
-template <int NT, class Layout>
-__device__ void rms_norm_to_smem(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w,
-                                 int n, float eps, uint16_t* __restrict__ out, float* red,
-                                 bool valid, Layout layout) {
-  const int tid = threadIdx.x;
-  if (!valid) {
-    for (int k = tid; k < n; k += NT) out[layout(k)] = 0;
-    return;
-  }
-  const bool vec = ((n & 7) == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0);
-  DF acc{0.0f, 0.0f};
-  if (vec) {
-    const uint4* xv = reinterpret_cast<const uint4*>(x);
-    for (int j = tid; j < n / 8; j += NT) {
-      const uint4 q = xv[j];
-      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo;
+}
+__device__ __forceinline__ float f2_hi(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return hi;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// BF16 pair (low half first) -> {f32(low), f32(high)}
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t u) {
+  return f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+
+// Two independent double-floats, packed: (hi.x, lo.x) and (hi.y, lo.y).
+struct DF2 {
+  uint64_t hi, lo;
+};
+// TwoSum of each lane's (hi, p), the error added to lo.
+__device__ __forceinline__ void df2_add(DF2& a, uint64_t p) {
+  const uint64_t s = f2_add(a.hi, p);
+  const uint64_t bp = f2_sub(s, a.hi);
+  const uint64_t e = f2_add(f2_sub(a.hi, f2_sub(s, bp)), f2_sub(p, bp));
+  a.hi = s;
+  a.lo = f2_add(a.lo, e);
+}
+__device__ __forceinline__ DF df2_x(const DF2& a) { return DF{f2_lo(a.hi), f2_lo(a.lo)}; }
+__device__ __forceinline__ DF df2_y(const DF2& a) { return DF{f2_hi(a.hi), f2_hi(a.lo)}; }
+
+// ------------------------------------------------------------------------------------------
+// rms_norm_vanilla prologue for several vectors at once:
+//   out_j = bf16( x_j * w_j / sqrt(mean(x_j^2) + eps) ), written into shared memory at layout(k).
+// The sums of squares are double-floats (each square of a BF16 value is exact in fp32), 1/rms is
+// formed in fp64 and split into two fp32 parts, and x*w (exact in fp32) times 1/rms is rounded
+// once to BF16 from a double-float -- so each output is the correctly rounded BF16 of the fp64
+// expression unless that lies within ~2^-40 relative of a rounding midpoint.
+// One pass over the inputs, one block reduction for all vectors. All NT threads of the block
+// call it; `red` holds >= njobs * (2 * NT / 32 + 2) floats. A job with valid == false writes
+// zeros without reading x.
+// ------------------------------------------------------------------------------------------
+struct NormJob {
+  const uint16_t* x;
+  const uint16_t* w;
+  uint16_t* out;
+  bool valid;
+};
+
+template <int NT, class Layout, class JobFn>
+__device__ void rms_norm_multi_to_smem(int njobs, int n, float eps, float* red, JobFn job,
+                                       Layout layout) {
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int j = 0; j < njobs; ++j) {
+    const NormJob J = job(j);
+    DF acc{0.0f, 0.0f};
+    if (J.valid) {
+      const bool vec = ((n & 7) == 0) && ((reinterpret_cast<uintptr_t>(J.x) & 15u) == 0);
+      if (vec) {
+        const uint4* xv = reinterpret_cast<const uint4*>(J.x);
+        for (int v = tid; v < n / 8; v += NT) {
+          const uint4 q = xv[v];
+          const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float a = bf16_lo(u[t]), b = bf16_hi(u[t]);
-        df_add(acc, __fmul_rn(a, a));
-        df_add(acc, __fmul_rn(b, b));
+          for (int t = 0; t < 4; ++t) {
+            const float a = bf16_lo(u[t]), b = bf16_hi(u[t]);
+            df_add(acc, __fmul_rn(a, a));
+            df_add(acc, __fmul_rn(b, b));
+          }
+        }
+      } else {
+        for (int k = tid; k < n; k += NT) {
+          const float a = bf16_bits_to_f32(J.x[k]);
+          df_add(acc, __fmul_rn(a, a));
+        }
       }
     }
-  } else {
-    for (int k = tid; k < n; k += NT) {
-      const float a = bf16_bits_to_f32(x[k]);
-      df_add(acc, __fmul_rn(a, a));
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) acc = df_add(acc, shfl_xor_df(acc, m));
+    if (lane == 0) {
+      red[(j * NW + warp) * 2] = acc.hi;
+      red[(j * NW + warp) * 2 + 1] = acc.lo;
     }
   }
-#pragma unroll
-  for (int m = 16; m > 0; m >>= 1) acc = df_add(acc, shfl_xor_df(acc, m));
-  const int warp = tid >> 5, lane = tid & 31;
-  if (lane == 0) {
-    red[2 * warp] = acc.hi;
-    red[2 * warp + 1] = acc.lo;
-  }
   __syncthreads();
-  if (tid == 0) {
-    DF tot{red[0], red[1]};
-    for (int i = 1; i < NT / 32; ++i) tot = df_add(tot, DF{red[2 * i], red[2 * i + 1]});
+  float* rr = red + njobs * NW * 2;
+  for (int j = tid; j < njobs; j += NT) {
+    DF tot{red[j * NW * 2], red[j * NW * 2 + 1]};
+    for (int i = 1; i < NW; ++i) tot = df_add(tot, DF{red[(j * NW + i) * 2], red[(j * NW + i) * 2 + 1]});
     const double ms = (static_cast<double>(tot.hi) + static_cast<double>(tot.lo)) / static_cast<double>(n);
     const double r = 1.0 / sqrt(ms + static_cast<double>(eps));
     const float rh = static_cast<float>(r);
-    const float rl = static_cast<float>(r - static_cast<double>(rh));
-    red[2 * (NT / 32)] = rh;
-    red[2 * (NT / 32) + 1] = rl;
+    rr[2 * j] = rh;
+    rr[2 * j + 1] = static_cast<float>(r - static_cast<double>(rh));
   }
   __syncthreads();
-  const float rh = red[2 * (NT / 32)], rl = red[2 * (NT / 32) + 1];
-  for (int k = tid; k < n; k += NT) {
-    const float p = __fmul_rn(bf16_bits_to_f32(x[k]), bf16_bits_to_f32(w[k]));  // exact
-    const float yh = __fmul_rn(p, rh);
-    const float ye = __fmaf_rn(p, rh, -yh);
-    const float yl = __fmaf_rn(p, rl, ye);
-    out[layout(k)] = bf16_rne_df(yh, yl);
+  for (int j = 0; j < njobs; ++j) {
+    const NormJob J = job(j);
+    const float rh = rr[2 * j], rl = rr[2 * j + 1];
+    const bool vec = ((n & 7) == 0) && ((reinterpret_cast<uintptr_t>(J.x) & 15u) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(J.w) & 15u) == 0);
+    if (vec) {
+      for (int v = tid; v < n / 8; v += NT) {
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+        if (J.valid) {
+          const uint4 xq = reinterpret_cast<const uint4*>(J.x)[v];
+          const uint4 wq = reinterpret_cast<const uint4*>(J.w)[v];
+          const uint32_t xu[4] = {xq.x, xq.y, xq.z, xq.w}, wu[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            uint32_t half[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float xe = h ? bf16_hi(xu[t]) : bf16_lo(xu[t]);
+              const float we = h ? bf16_hi(wu[t]) : bf16_lo(wu[t]);
+              const float p = __fmul_rn(xe, we);  // exact
+              const float yh = __fmul_rn(p, rh);
+              const float yl = __fmaf_rn(p, rl, __fmaf_rn(p, rh, -yh));
+              half[h] = bf16_rne_df(yh, yl);
+            }
+            o[t] = half[0] | (half[1] << 16);
+          }
+        }
+        // 8 consecutive elements starting at a multiple of 8 stay consecutive in every layout
+        *reinterpret_cast<uint4*>(J.out + layout(8 * v)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    } else {
+      for (int k = tid; k < n; k += NT) {
+        uint16_t o = 0;
+        if (J.valid) {
+          const float p = __fmul_rn(bf16_bits_to_f32(J.x[k]), bf16_bits_to_f32(J.w[k]));
+          const float yh = __fmul_rn(p, rh);
+          const float yl = __fmaf_rn(p, rl, __fmaf_rn(p, rh, -yh));
+          o = bf16_rne_df(yh, yl);
+        }
+        J.out[layout(k)] = o;
+      }
+    }
   }
 }
 

@@ -2,18 +2,19 @@
 // the embedding row read by pointer at token*hidden, `norm` with enorm into concat[0:H] and
 // with hnorm into concat[H:2H], then the `eh_proj` dense gemv, n = H, k = 2H).
 //
-// Design: the same persistent, per-warp TMA-pipelined row stream as the output stage, here over
-// the [H, 2H] eh_proj rows. The gather is an address computation on the device-resident token
-// (so a draft chain or a CUDA graph can feed the previous draft straight back in), and every
-// CTA builds the normalised concat for its B sequences in shared memory while its first weight
-// stages are already in flight.
+// Design: the same persistent, per-warp bulk-copy row stream as the output stage, here over the
+// [H, 2H] eh_proj rows. The gather is an address computation on the device-resident token (so
+// a draft chain or a CUDA graph can feed the previous draft straight back in), and every CTA
+// builds the normalised concat of its B sequences in shared memory (one pass, one block
+// reduction for all 2B norms) while its first weight stages are already in flight.
 //
 // Accuracy: x is rounded to BF16 right after this sum, so the sum is error-free up to the final
 // rounding: every product of two BF16 values is exact in fp32, and each one is added to a
-// per-lane double-float (hi, lo) with TwoSum (four independent accumulators per lane, element
-// e going to e % 4); accumulators and lanes are combined the same way and the value is rounded
-// once to BF16. x therefore equals the BF16 rounding of the exact sum unless that sum lies
-// within ~2^-40 relative of a rounding midpoint.
+// double-float (hi, lo) with TwoSum -- four packed f32x2 double-floats per lane and sequence,
+// element pair (2u, 2u+1) of a 16-byte vector going to pair u; the eight double-floats and
+// then the lanes are combined the same way and the value is rounded once to BF16. x therefore
+// equals the BF16 rounding of the exact sum unless that lies within ~2^-40 (relative) of a
+// rounding midpoint.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,29 +27,57 @@ namespace {
 
 __device__ __forceinline__ bool token_ok(int32_t tok, int V) { return tok >= 0 && tok < V; }
 
-// Build c_b = [enorm(embed[tok_b]) | hnorm(hidden_b)] for all sequences into shared memory.
-template <int NB_MAX>
-__device__ void build_concat(const InputArgs& a, int nb, uint16_t* vec, int vec_elems, float* red,
-                             bool* valid) {
+// Build c_b = [enorm(embed[tok_b]) | hnorm(hidden_b)] for sequences b0 .. b0+nb-1 into shared
+// memory (slot b - b0); valid[slot] says whether the token was in range.
+template <int NT>
+__device__ void build_concat(const InputArgs& a, int b0, int nb, uint16_t* vec, int vec_elems,
+                             float* red, bool* valid) {
   const int H = a.H;
-  for (int b = 0; b < nb; ++b) {
-    const int32_t tok = a.tokens[b];
-    const bool ok = token_ok(tok, a.V);
-    valid[b] = ok;
-    if (!ok && threadIdx.x == 0) store_status(a.status, MTP_ERR_TOKEN_RANGE);
-    uint16_t* cb = vec + static_cast<size_t>(b) * vec_elems;
-    const uint16_t* erow = ok ? a.embed + static_cast<int64_t>(tok) * H : a.embed;
-    rms_norm_to_smem<kThreads>(erow, a.enorm_w, H, a.eps, cb, red, ok, LayoutIdentity{});
-    __syncthreads();
-    rms_norm_to_smem<kThreads>(a.hidden + static_cast<size_t>(b) * H, a.hnorm_w, H, a.eps, cb + H,
-                               red, true, LayoutIdentity{});
-    __syncthreads();
+  if (threadIdx.x < nb) {
+    const bool ok = token_ok(a.tokens[b0 + threadIdx.x], a.V);
+    valid[threadIdx.x] = ok;
+    if (!ok) store_status(a.status, MTP_ERR_TOKEN_RANGE);
+  }
+  __syncthreads();
+  auto job = [&](int j) {
+    const int i = j >> 1, b = b0 + i;
+    uint16_t* cb = vec + static_cast<size_t>(i) * vec_elems;
+    if ((j & 1) == 0) {
+      const bool ok = valid[i];
+      const uint16_t* erow = ok ? a.embed + static_cast<int64_t>(a.tokens[b]) * H : a.embed;
+      return NormJob{erow, a.enorm_w, cb, ok};
+    }
+    return NormJob{a.hidden + static_cast<size_t>(b) * H, a.hnorm_w, cb + H, true};
+  };
+  rms_norm_multi_to_smem<NT>(2 * nb, H, a.eps, red, job, LayoutIdentity{});
+  __syncthreads();
+}
+
+// Exact products of one 16-byte weight vector (4 BF16 pairs) with the concat, added to the
+// four packed double-floats of one sequence (independent chains).
+__device__ __forceinline__ void dot8_exact(const uint4& w, const uint4& c, DF2 (&acc)[4]) {
+  const uint32_t wu[4] = {w.x, w.y, w.z, w.w};
+  const uint32_t cu[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+#if MTP_MIXED_FMA
+    float p0, p1;
+    asm("{\n\t.reg .b16 wl, wh, cl, ch;\n\t.reg .f32 z;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\tmov.b32 {cl, ch}, %3;\n\tmov.f32 z, 0f00000000;\n\t"
+        "fma.rn.f32.bf16 %0, wl, cl, z;\n\tfma.rn.f32.bf16 %1, wh, ch, z;\n\t}"
+        : "=f"(p0), "=f"(p1)
+        : "r"(wu[u]), "r"(cu[u]));
+    const uint64_t p = f2_pack(p0, p1);
+#else
+    const uint64_t p = f2_mul(bf16x2_to_f2(wu[u]), bf16x2_to_f2(cu[u]));  // exact products
+#endif
+    df2_add(acc[u], p);
   }
 }
 
-template <int NB>
-__global__ void __launch_bounds__(kThreads, 1) input_tma_kernel(const InputArgs a) {
-  constexpr int NW = kWarps;
+template <int NB, int NWI>
+__global__ void __launch_bounds__(NWI * 32, 1) input_tma_kernel(const InputArgs a) {
+  constexpr int NW = NWI;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ bool valid_s[kMaxB];
 
@@ -99,17 +128,18 @@ __global__ void __launch_bounds__(kThreads, 1) input_tma_kernel(const InputArgs 
 
   // tokens and target_hidden may come from the preceding kernel
   pdl_wait_prior_grid();
-  build_concat<NB>(a, NB, vec, vec_elems, red, valid_s);
+  build_concat<NW * 32>(a, 0, NB, vec, vec_elems, red, valid_s);
   bool valid[NB];
 #pragma unroll
   for (int b = 0; b < NB; ++b) valid[b] = valid_s[b];
   pdl_launch_dependents();
 
-  DF acc[NB][4];
+  const uint64_t zero2 = f2_pack(0.0f, 0.0f);
+  DF2 acc[NB][4];
 #pragma unroll
   for (int b = 0; b < NB; ++b)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[b][e] = DF{0.0f, 0.0f};
+    for (int u = 0; u < 4; ++u) acc[b][u] = DF2{zero2, zero2};
   int ci = 0, cc = 0, cs = 0, t_fail = -1;
   uint32_t parity = 0;
   for (int t = 0; t < nitems; ++t) {
@@ -124,15 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1) input_tma_kernel(const InputArgs 
 #pragma unroll 2
     for (int j = lane; j < nv; j += 32) {
       const uint4 q = wv[j];
-      const float wf[8] = {bf16_lo(q.x), bf16_hi(q.x), bf16_lo(q.y), bf16_hi(q.y),
-                           bf16_lo(q.z), bf16_hi(q.z), bf16_lo(q.w), bf16_hi(q.w)};
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         const uint4 cq = reinterpret_cast<const uint4*>(vec + static_cast<size_t>(b) * vec_elems)[J0 + j];
-        const float cf[8] = {bf16_lo(cq.x), bf16_hi(cq.x), bf16_lo(cq.y), bf16_hi(cq.y),
-                             bf16_lo(cq.z), bf16_hi(cq.z), bf16_lo(cq.w), bf16_hi(cq.w)};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) df_add(acc[b][e & 3], __fmul_rn(wf[e], cf[e]));  // exact product
+        dot8_exact(q, cq, acc[b]);
       }
     }
     __syncwarp();
@@ -147,17 +172,19 @@ __global__ void __launch_bounds__(kThreads, 1) input_tma_kernel(const InputArgs 
       ++ci;
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        DF v = df_add(df_add(acc[b][0], acc[b][1]), df_add(acc[b][2], acc[b][3]));
+        DF v = df_add(df_add(df_add(df2_x(acc[b][0]), df2_y(acc[b][0])), df_add(df2_x(acc[b][1]), df2_y(acc[b][1]))),
+                      df_add(df_add(df2_x(acc[b][2]), df2_y(acc[b][2])), df_add(df2_x(acc[b][3]), df2_y(acc[b][3]))));
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) v = df_add(v, shfl_xor_df(v, m));
         if (lane == 0) a.x[static_cast<size_t>(b) * H + row] = valid[b] ? bf16_rne_df(v.hi, v.lo) : uint16_t(0);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[b][e] = DF{0.0f, 0.0f};
+        for (int u = 0; u < 4; ++u) acc[b][u] = DF2{zero2, zero2};
       }
     }
   }
   if (t_fail >= 0 && lane == 0) {
     store_status(a.status, MTP_ERR_TIMEOUT);
+    // let the copies still in flight land before the CTA's shared memory is released
     int s = cs;
     uint32_t par = parity;
     for (int u = t_fail; u < nitems && u < t_fail + S; ++u) {
@@ -167,40 +194,50 @@ __global__ void __launch_bounds__(kThreads, 1) input_tma_kernel(const InputArgs 
   }
 }
 
-// Plain-load input stage for any H and B <= 16: one warp per output row.
+// Plain-load input stage for any H and B <= 16: one warp per output row. The concat of
+// `group` sequences is resident at a time; larger batches take several passes over eh_proj.
 __global__ void __launch_bounds__(kThreads) input_plain_kernel(const InputArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ bool valid_s[kMaxB];
-  const int H = a.H, K = 2 * H, nb = a.B;
+  const int H = a.H, K = 2 * H, group = a.group;
   const int vec_elems = ((K + 7) / 8) * 8;
   uint16_t* vec = reinterpret_cast<uint16_t*>(smem);
-  float* red = reinterpret_cast<float*>(vec + static_cast<size_t>(nb) * vec_elems);
+  float* red = reinterpret_cast<float*>(vec + static_cast<size_t>(group) * vec_elems);
 
   pdl_wait_prior_grid();
-  build_concat<kMaxB>(a, nb, vec, vec_elems, red, valid_s);
-  pdl_launch_dependents();
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const int64_t tw = static_cast<int64_t>(gridDim.x) * kWarps;
-  for (int64_t row = gw; row < H; row += tw) {
-    const uint16_t* wr = a.eh_proj + row * K;
-    for (int b = 0; b < nb; ++b) {
-      const uint16_t* cb = vec + static_cast<size_t>(b) * vec_elems;
-      DF acc{0.0f, 0.0f};
-      for (int k = lane; k < K; k += 32)
-        df_add(acc, __fmul_rn(bf16_bits_to_f32(wr[k]), bf16_bits_to_f32(cb[k])));
-      for (int m = 16; m > 0; m >>= 1) acc = df_add(acc, shfl_xor_df(acc, m));
-      if (lane == 0) a.x[static_cast<size_t>(b) * H + row] = valid_s[b] ? bf16_rne_df(acc.hi, acc.lo) : uint16_t(0);
+  for (int b0 = 0; b0 < a.B; b0 += group) {
+    const int nb = (a.B - b0) < group ? (a.B - b0) : group;
+    __syncthreads();  // the previous group's concat is no longer read
+    build_concat<kThreads>(a, b0, nb, vec, vec_elems, red, valid_s);
+    for (int64_t row = gw; row < H; row += tw) {
+      const uint16_t* wr = a.eh_proj + row * K;
+      for (int i = 0; i < nb; ++i) {
+        const uint16_t* cb = vec + static_cast<size_t>(i) * vec_elems;
+        DF acc{0.0f, 0.0f};
+        for (int k = lane; k < K; k += 32)
+          df_add(acc, __fmul_rn(bf16_bits_to_f32(wr[k]), bf16_bits_to_f32(cb[k])));
+        for (int m = 16; m > 0; m >>= 1) acc = df_add(acc, shfl_xor_df(acc, m));
+        if (lane == 0)
+          a.x[static_cast<size_t>(b0 + i) * H + row] = valid_s[i] ? bf16_rne_df(acc.hi, acc.lo) : uint16_t(0);
+      }
     }
   }
+  pdl_launch_dependents();
 }
 
-cudaError_t launch_input_kernel(void (*kernel)(InputArgs), unsigned grid, size_t smem,
+cudaError_t launch_input_kernel(void (*kernel)(InputArgs), unsigned grid, unsigned threads, size_t smem,
                                 cudaStream_t stream, InputArgs a) {
   void* args[] = {&a};
-  return launch_pdl(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(kThreads), smem, stream, args);
+  return launch_pdl(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(threads), smem, stream, args);
 }
+
+#ifndef MTP_INPUT_WARPS
+#define MTP_INPUT_WARPS 16
+#endif
+constexpr int kInWarps = MTP_INPUT_WARPS;
 
 }  // namespace
 
@@ -210,15 +247,15 @@ cudaError_t launch_input_stage(const InputArgs& in, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   InputArgs a = in;
   const int K = 2 * a.H;
-  const int64_t want = (static_cast<int64_t>(a.H) + kWarps - 1) / kWarps;
-  int64_t grid = di.sm_count < want ? di.sm_count : want;
-  if (grid < 1) grid = 1;
-  const size_t misc = static_cast<size_t>(2 * kWarps + 2) * sizeof(float) + 256;
+  const size_t misc = kRedBytes + 256;
   const bool rows16 = (K % 8) == 0;
   if (rows16 && a.B <= kTmaMaxB) {
+    const int64_t want = (static_cast<int64_t>(a.H) + kInWarps - 1) / kInWarps;
+    int64_t grid = di.sm_count < want ? di.sm_count : want;
+    if (grid < 1) grid = 1;
     const int vec_elems = ((K / 8 + 31) / 32) * 32 * 8;
     const size_t fixed = static_cast<size_t>(a.B) * vec_elems * 2 + misc;
-    const size_t per_stage = static_cast<size_t>(kWarps) * (kChunk + 8);
+    const size_t per_stage = static_cast<size_t>(kInWarps) * (kChunk + 8);
     if (fixed + 2 * per_stage <= static_cast<size_t>(di.smem_optin)) {
       int S = static_cast<int>((static_cast<size_t>(di.smem_optin) - fixed) / per_stage);
       if (S > kMaxStages) S = kMaxStages;
@@ -226,19 +263,26 @@ cudaError_t launch_input_stage(const InputArgs& in, cudaStream_t stream) {
       const size_t smem = fixed + static_cast<size_t>(S) * per_stage;
       void (*k)(InputArgs) = nullptr;
       switch (a.B) {
-        case 1: k = input_tma_kernel<1>; break;
-        case 2: k = input_tma_kernel<2>; break;
-        case 3: k = input_tma_kernel<3>; break;
-        default: k = input_tma_kernel<4>; break;
+        case 1: k = input_tma_kernel<1, kInWarps>; break;
+        case 2: k = input_tma_kernel<2, kInWarps>; break;
+        case 3: k = input_tma_kernel<3, kInWarps>; break;
+        default: k = input_tma_kernel<4, kInWarps>; break;
       }
-      return launch_input_kernel(k, static_cast<unsigned>(grid), smem, stream, a);
+      return launch_input_kernel(k, static_cast<unsigned>(grid), kInWarps * 32, smem, stream, a);
     }
   }
+  const int64_t want = (static_cast<int64_t>(a.H) + kWarps - 1) / kWarps;
+  int64_t grid = di.sm_count < want ? di.sm_count : want;
+  if (grid < 1) grid = 1;
   const int vec_elems = ((K + 7) / 8) * 8;
-  const size_t smem = static_cast<size_t>(a.B) * vec_elems * 2 + misc;
-  if (smem > static_cast<size_t>(di.smem_optin)) return cudaErrorNotSupported;
+  const size_t per_seq = static_cast<size_t>(vec_elems) * 2;
+  if (misc + per_seq > static_cast<size_t>(di.smem_optin)) return cudaErrorNotSupported;
+  int group = static_cast<int>((static_cast<size_t>(di.smem_optin) - misc) / per_seq);
+  if (group > a.B) group = a.B;
   a.stages = 0;
-  return launch_input_kernel(input_plain_kernel, static_cast<unsigned>(grid), smem, stream, a);
+  a.group = group;
+  const size_t smem = static_cast<size_t>(group) * per_seq + misc;
+  return launch_input_kernel(input_plain_kernel, static_cast<unsigned>(grid), kThreads, smem, stream, a);
 }
 
 }  // namespace mtp

@@ -18,7 +18,10 @@ namespace mtp {
 #define MTP_MAX_STAGES 6
 #endif
 #ifndef MTP_MIXED_FMA
-#define MTP_MIXED_FMA 0
+#define MTP_MIXED_FMA 1
+#endif
+#ifndef MTP_REGX
+#define MTP_REGX 1
 #endif
 
 constexpr int kWarps = MTP_WARPS;
@@ -28,6 +31,8 @@ constexpr int kMaxStages = MTP_MAX_STAGES;
 constexpr int kTmaMaxB = 4;              // the CUDA-core streaming kernels take B <= 4
 
 constexpr int kSmemReserve = 1024;      // opt-in bytes kept back for static shared variables
+// shared scratch of the norm prologue: up to 2 * 16 vectors, (2 * warps + 2) floats each
+constexpr size_t kRedBytes = sizeof(float) * 2 * 16 * (2 * kWarps + 2);
 
 struct DeviceInfo {
   int sm_count;
@@ -53,7 +58,8 @@ struct InputArgs {
   int32_t* status;
   int B, H, V;
   float eps;
-  int stages;
+  int stages;  // pipeline stages (bulk-copy kernel)
+  int group;   // sequences whose concat is resident at once (plain kernel)
 };
 
 struct SweepArgs {

@@ -366,3 +366,31 @@ def test_short_chain_teacher_forced():
         out = oracle.head(c.wb, [tok], _bits(hiddens[i].cpu()), EPS)
         check_draft(drafts_graph[i], None, out["logits"][0], TOL_BF16)
         tok = drafts_graph[i]  # teacher-forced: the oracle follows the GPU's token
+
+
+@pytest.mark.parametrize("H", [6144, 2048, 96])
+def test_fp8_every_code_including_subnormals(H):
+    # rows made of every finite E4M3 code (subnormals 0x01..0x07 included) with unit-ish scales:
+    # the logits depend on each code's exact value, so a decode that lost subnormals would show
+    V = 300
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    rng = np.random.default_rng(H)
+    Q = codes[rng.integers(0, codes.size, (V, H))].astype(np.uint8)
+    Q[0] = 0x01          # a row of only the smallest subnormal
+    Q[1, ::2] = 0x07     # the largest subnormal, alternating with zero
+    Q[1, 1::2] = 0x00
+    s = rng.uniform(0.5, 2.0, V).astype(np.float32)
+    x = synth._normal_bf16((1, H), 0.0, 1.0, torch.Generator().manual_seed(H), "cpu")
+    fw = synth._normal_bf16((H,), 1.0, 0.1, torch.Generator().manual_seed(H + 1), "cpu")
+    xhat = oracle.final_norm(_bits(x), _bits(fw), EPS)
+    ref = oracle.logits(1, Q, s, xhat).reshape(1, -1)
+    ws = m.workspace(1, H, V, DEV)
+    logits = torch.empty((1, V), dtype=torch.float32, device=DEV)
+    draft = torch.empty(1, dtype=torch.int32, device=DEV)
+    m.mtp_head_logits_argmax(x.to(DEV), fw.to(DEV), torch.from_numpy(Q).to(DEV), torch.from_numpy(s).to(DEV),
+                             m.W_FP8_E4M3, logits, draft, ws)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(lg, ref, rtol=1e-4, atol=1e-6 * np.abs(ref).max())
+    assert lg[0, 0] != 0.0 and lg[0, 1] != 0.0
+    check_logits_and_draft(logits.cpu().numpy(), draft.cpu().numpy(), ref, TOL_FP8)
