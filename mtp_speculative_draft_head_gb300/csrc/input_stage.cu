@@ -250,25 +250,36 @@ cudaError_t launch_input_stage(const InputArgs& in, cudaStream_t stream) {
   const size_t misc = kRedBytes + 256;
   const bool rows16 = (K % 8) == 0;
   if (rows16 && a.B <= kTmaMaxB) {
-    const int64_t want = (static_cast<int64_t>(a.H) + kInWarps - 1) / kInWarps;
-    int64_t grid = di.sm_count < want ? di.sm_count : want;
-    if (grid < 1) grid = 1;
+    // the widest warp count whose stages fit next to the concat of B sequences
     const int vec_elems = ((K / 8 + 31) / 32) * 32 * 8;
     const size_t fixed = static_cast<size_t>(a.B) * vec_elems * 2 + misc;
-    const size_t per_stage = static_cast<size_t>(kInWarps) * (kChunk + 8);
-    if (fixed + 2 * per_stage <= static_cast<size_t>(di.smem_optin)) {
+    for (int nwi : {kInWarps, kWarps}) {
+      const size_t per_stage = static_cast<size_t>(nwi) * (kChunk + 8);
+      if (fixed + 2 * per_stage > static_cast<size_t>(di.smem_optin)) continue;
+      const int64_t want = (static_cast<int64_t>(a.H) + nwi - 1) / nwi;
+      int64_t grid = di.sm_count < want ? di.sm_count : want;
+      if (grid < 1) grid = 1;
       int S = static_cast<int>((static_cast<size_t>(di.smem_optin) - fixed) / per_stage);
       if (S > kMaxStages) S = kMaxStages;
       a.stages = S;
       const size_t smem = fixed + static_cast<size_t>(S) * per_stage;
       void (*k)(InputArgs) = nullptr;
-      switch (a.B) {
-        case 1: k = input_tma_kernel<1, kInWarps>; break;
-        case 2: k = input_tma_kernel<2, kInWarps>; break;
-        case 3: k = input_tma_kernel<3, kInWarps>; break;
-        default: k = input_tma_kernel<4, kInWarps>; break;
+      if (nwi == kInWarps) {
+        switch (a.B) {
+          case 1: k = input_tma_kernel<1, kInWarps>; break;
+          case 2: k = input_tma_kernel<2, kInWarps>; break;
+          case 3: k = input_tma_kernel<3, kInWarps>; break;
+          default: k = input_tma_kernel<4, kInWarps>; break;
+        }
+      } else {
+        switch (a.B) {
+          case 1: k = input_tma_kernel<1, kWarps>; break;
+          case 2: k = input_tma_kernel<2, kWarps>; break;
+          case 3: k = input_tma_kernel<3, kWarps>; break;
+          default: k = input_tma_kernel<4, kWarps>; break;
+        }
       }
-      return launch_input_kernel(k, static_cast<unsigned>(grid), kInWarps * 32, smem, stream, a);
+      return launch_input_kernel(k, static_cast<unsigned>(grid), nwi * 32, smem, stream, a);
     }
   }
   const int64_t want = (static_cast<int64_t>(a.H) + kWarps - 1) / kWarps;

@@ -341,13 +341,20 @@ __global__ void __launch_bounds__(NWR * 32, 1) sweep_regx_kernel(const SweepArgs
   for (int j = 0; j < kGroup; ++j) part[j] = 0.0f;
   int cs = 0, i_fail = -1;
   uint32_t parity = 0;
-  float my_scale = 1.0f;
+  // row scales of this lane's slot, loaded one group ahead so the load is off the critical path
+  float my_scale = 1.0f, next_scale = 1.0f;
+  if constexpr (WT == MTP_W_FP8_E4M3) {
+    if (my_slot < nrows) next_scale = __ldg(a.scale + r0 + warp + static_cast<int64_t>(my_slot) * NWR);
+  }
 #pragma unroll 1
   for (int i = 0; i < nrows; ++i) {
     const int jj = i & (kGroup - 1);
     if constexpr (WT == MTP_W_FP8_E4M3) {
-      if (jj == 0 && i + my_slot < nrows)
-        my_scale = __ldg(a.scale + r0 + warp + static_cast<int64_t>(i + my_slot) * NWR);
+      if (jj == 0) {
+        my_scale = next_scale;
+        const int nxt = i + kGroup + my_slot;
+        if (nxt < nrows) next_scale = __ldg(a.scale + r0 + warp + static_cast<int64_t>(nxt) * NWR);
+      }
     }
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&my_bars[cs]), parity))) {
       i_fail = i;
@@ -610,7 +617,7 @@ cudaError_t launch_tma(SweepArgs a, const DeviceInfo& di, unsigned grid, size_t 
 #define MTP_REGX_WARPS_BF16 8
 #endif
 #ifndef MTP_REGX_WARPS_FP8
-#define MTP_REGX_WARPS_FP8 8
+#define MTP_REGX_WARPS_FP8 12
 #endif
 #ifndef MTP_FP8_CVT
 #define MTP_FP8_CVT 1
