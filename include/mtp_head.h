@@ -126,6 +126,29 @@ int mtp_head_logits_argmax(const uint16_t* x, const uint16_t* final_norm_w, cons
                            int32_t* status, void* workspace, size_t workspace_bytes, int H,
                            int V, float eps, void* stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Output stage without a caller-provided workspace. The source pages have no counterpart: this
+ * entry point exists for callers of this library that cannot allocate device memory -- e.g. a
+ * plug-in that only receives the buffers its host framework hands it and has no allocator of
+ * its own, or a process whose device memory was all claimed up front by another allocator.
+ * It computes exactly what mtp_head_logits_argmax_batched computes (same kernels, same
+ * arguments minus workspace / workspace_bytes) and allocates nothing: the workspace is a fixed
+ * device array inside the library, 131,200 bytes, enough for the largest batch (B <= 16);
+ * every GPU that loads the library holds it until the process exits. B outside 1..16 returns
+ * MTP_ERR_SHAPE before anything runs.
+ *   - The first call on a device looks up that array's device address (once per device, with
+ *     the device current). Make that first call before any stream capture on the device.
+ *   - All calls share the one array. The call clears its counter on `stream` before launching,
+ *     so it never depends on what a previous call left there, but calls that may run at the
+ *     same time on the GPU (different streams, or different host threads) race on it: order
+ *     them on one stream or use mtp_head_logits_argmax_batched with separate workspaces.
+ * ---------------------------------------------------------------------------------------- */
+int mtp_head_logits_argmax_batched_noalloc(const uint16_t* x, const uint16_t* final_norm_w,
+                                           const void* lm_head, const float* row_scale,
+                                           int w_dtype, float* logits, int32_t* draft,
+                                           int32_t* status, int B, int H, int V, float eps,
+                                           void* stream);
+
 /* Bytes of workspace the output stage needs (no device query; 0 for invalid shapes). */
 size_t mtp_head_workspace_bytes(int B, int H, int V);
 

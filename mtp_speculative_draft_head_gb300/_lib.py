@@ -37,6 +37,7 @@ SIGNATURES = {
     "mtp_head_input": (I, [P, P, P, P, P, P, P, P, I, I, F, P]),
     "mtp_head_logits_argmax_batched": (I, [P, P, P, P, I, P, P, P, P, Z, I, I, I, F, P]),
     "mtp_head_logits_argmax": (I, [P, P, P, P, I, P, P, P, P, Z, I, I, F, P]),
+    "mtp_head_logits_argmax_batched_noalloc": (I, [P, P, P, P, I, P, P, P, I, I, I, F, P]),
     "mtp_head_workspace_bytes": (Z, [I, I, I]),
     "mtp_head_forward_batched": (I, [P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, Z, I, I, I, F, P]),
     "mtp_head_forward_host": (I, [P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, P, P, Z, I, I, I, F, P]),
@@ -159,6 +160,20 @@ def mtp_head_logits_argmax(x, final_norm_w, lm_head, row_scale, w_dtype: int, lo
         _dev(status, "status"), _dev(ws, "workspace"), ws.numel() * ws.element_size(), H, V, eps,
         _stream(stream)),
         "mtp_head_logits_argmax")
+
+
+def mtp_head_logits_argmax_batched_noalloc(x, final_norm_w, lm_head, row_scale, w_dtype: int,
+                                           logits, draft, status=None, eps: float = 1e-6,
+                                           stream=None) -> None:
+    """Output stage on the library's own fixed device scratch (no workspace argument): for
+    callers that cannot allocate device memory. Calls that overlap on the GPU race on it."""
+    V, H = lm_head.shape
+    B = draft.numel()
+    _check(load().mtp_head_logits_argmax_batched_noalloc(
+        _dev(x, "x"), _dev(final_norm_w, "final_norm_w"), _dev(lm_head, "lm_head"),
+        _dev(row_scale, "row_scale"), int(w_dtype), _dev(logits, "logits"), _dev(draft, "draft"),
+        _dev(status, "status"), B, H, V, eps, _stream(stream)),
+        "mtp_head_logits_argmax_batched_noalloc")
 
 
 def mtp_head_forward_batched(embed, enorm_w, hnorm_w, eh_proj, final_norm_w, lm_head, row_scale,

@@ -102,6 +102,17 @@ int run_output(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_h
 
 }  // namespace
 
+namespace mtp {
+// The output stage's host-side argument check, for other entry points of this library.
+int check_output_args(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_head,
+                      const float* row_scale, int w_dtype, const float* logits, const int32_t* draft,
+                      const int32_t* status, const void* workspace, size_t workspace_bytes, int B,
+                      int H, int V, float eps) {
+  return validate_output(x, final_norm_w, lm_head, row_scale, w_dtype, logits, draft, status,
+                         workspace, workspace_bytes, B, H, V, eps);
+}
+}  // namespace mtp
+
 extern "C" {
 
 int mtp_head_input_batched(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hnorm_w,

@@ -82,6 +82,12 @@ cudaError_t launch_sweep(const SweepArgs& a, cudaStream_t stream);
 cudaError_t launch_quantize(const uint16_t* w, uint8_t* q, float* scale, int32_t* status,
                             int V, int H, cudaStream_t stream);
 
+// Host-side argument check of the output stage (status code, nothing launched).
+int check_output_args(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_head,
+                      const float* row_scale, int w_dtype, const float* logits, const int32_t* draft,
+                      const int32_t* status, const void* workspace, size_t workspace_bytes, int B,
+                      int H, int V, float eps);
+
 // Workspace layout of the output stage: a 128-byte header (the CTA completion counter), then
 // one (value, index) partial per CTA and sequence.
 size_t sweep_workspace_bytes(int B);
