@@ -315,7 +315,7 @@ def run_ours(args, world, rank, local):
     e2e_gbs = step_bytes(2) * ke * world / (e2e_ms * 1e-3) / 1e9
 
     peak, peak_src = peak_hbm()
-    kname = "sweep_tma_kernel<BF16,B=1>"
+    kname = "sweep_regx_kernel<BF16,H=6144,B=1>"
     achieved = sweep_bytes(2) / (results[("sweep", False)] / K * 1e-3) / 1e9
     line = {
         "metric": METRIC,
