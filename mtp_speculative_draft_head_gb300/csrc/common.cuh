@@ -92,6 +92,34 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
       : "memory");
 }
 
+// 2-D tensor tile global -> shared through the TMA engine (tensor map in kernel parameter space),
+// completing on mbarrier `bar`. x (innermost coordinate) must start on a 16-byte boundary.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar,
+                                           uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Barrier over a subset of the block's warps (hardware named barrier `id`, `nthreads` threads).
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Programmatic dependent launch: wait for the preceding grid (no-op when the launch did not
 // ask for it), and allow the next grid to be scheduled.
 __device__ __forceinline__ void pdl_wait_prior_grid() {
@@ -171,6 +199,61 @@ __device__ __forceinline__ uint16_t bf16_rne_df(float hi, float lo) {
     up = ((__float_as_uint(e) ^ u) & 0x80000000u) == 0u;  // same sign: larger magnitude
   }
   return static_cast<uint16_t>(base + (up ? 1u : 0u));
+}
+
+// BF16 (round to nearest even) of the double-float p * (rh + rl) as bf16_rne_df(yh, yl) with
+// yh = fl(p * rh), yl = fl(p * rl + (p * rh - yh)) -- bit for bit, but cheaper: |yl| stays below
+// 1.5 fp32 ulps of yh (|p * rh - yh| <= 0.5 ulp, |p * rl| < 1 ulp since |rl| <= ulp(rh) / 2), so
+// the BF16 rounding of yh + yl can differ from that of yh alone only when yh lies within a few
+// fp32 ulps of a BF16 midpoint (low 16 bits 0x7FFE..0x8002); those, inf / NaN, and a
+// subnormal rh (where |rl| <= ulp(rh) / 2 no longer bounds p * rl by an ulp of yh) take the
+// exact path.
+// (The exact path is out of line: inlined into every element it doubled the cost of the
+// common one.)
+static __device__ __noinline__ uint32_t bf16_scaled_rne_exact(float p, float rh, float rl) {
+  const float yh = __fmul_rn(p, rh);
+  const float yl = __fmaf_rn(p, rl, __fmaf_rn(p, rh, -yh));
+  return bf16_rne_df(yh, yl);
+}
+__device__ __forceinline__ uint32_t bf16_scaled_rne(float p, float rh, float rl) {
+  const float yh = __fmul_rn(p, rh);
+  const uint32_t u = __float_as_uint(yh);
+  if (((u & 0xFFFFu) - 0x7FFEu) <= 4u || (u & 0x7F800000u) == 0x7F800000u || !(rh >= 1.17549435e-38f))
+    return bf16_scaled_rne_exact(p, rh, rl);
+  unsigned short h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(yh));
+  return h;
+}
+
+// Eight values at once: BF16 of x_i * w_i * (rh + rl) for the BF16 pairs xu[t] (elements 2t,
+// 2t+1) and fp32 weights wf[i], packed in pairs -- the same bits as bf16_scaled_rne per element.
+// The common path is straight-line (one packed conversion per pair); a cell with any element
+// near a midpoint, inf / NaN, or a subnormal rh is redone on the exact path as a whole.
+__device__ __forceinline__ uint4 bf16x8_scaled_rne(const uint32_t (&xu)[4], const float (&wf)[8], float rh,
+                                                   float rl) {
+  float p[8], y[8];
+  uint32_t flag = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    p[i] = __fmul_rn((i & 1) ? bf16_hi(xu[i >> 1]) : bf16_lo(xu[i >> 1]), wf[i]);  // exact
+    y[i] = __fmul_rn(p[i], rh);
+    const uint32_t u = __float_as_uint(y[i]);
+    flag |= static_cast<uint32_t>(((u - 0x7FFEu) & 0xFFFFu) <= 4u) | static_cast<uint32_t>((u & 0x7F800000u) == 0x7F800000u);
+  }
+  uint32_t o[4];
+  if (flag == 0u && rh >= 1.17549435e-38f) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[t]) : "f"(y[2 * t + 1]), "f"(y[2 * t]));
+  } else {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float h0 = y[2 * t], h1 = y[2 * t + 1];
+      const float l0 = __fmaf_rn(p[2 * t], rl, __fmaf_rn(p[2 * t], rh, -h0));
+      const float l1 = __fmaf_rn(p[2 * t + 1], rl, __fmaf_rn(p[2 * t + 1], rh, -h1));
+      o[t] = static_cast<uint32_t>(bf16_rne_df(h0, l0)) | (static_cast<uint32_t>(bf16_rne_df(h1, l1)) << 16);
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // E4M3 byte i (0..3) of a 32-bit word -> fp32 holding value * 2^-120, exactly.
@@ -334,42 +417,94 @@ __device__ void rms_norm_multi_to_smem(int njobs, int n, float eps, float* red, 
                      ((reinterpret_cast<uintptr_t>(J.w) & 15u) == 0);
     if (vec) {
       for (int v = tid; v < n / 8; v += NT) {
-        uint32_t o[4] = {0u, 0u, 0u, 0u};
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
         if (J.valid) {
           const uint4 xq = reinterpret_cast<const uint4*>(J.x)[v];
           const uint4 wq = reinterpret_cast<const uint4*>(J.w)[v];
-          const uint32_t xu[4] = {xq.x, xq.y, xq.z, xq.w}, wu[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            uint32_t half[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const float xe = h ? bf16_hi(xu[t]) : bf16_lo(xu[t]);
-              const float we = h ? bf16_hi(wu[t]) : bf16_lo(wu[t]);
-              const float p = __fmul_rn(xe, we);  // exact
-              const float yh = __fmul_rn(p, rh);
-              const float yl = __fmaf_rn(p, rl, __fmaf_rn(p, rh, -yh));
-              half[h] = bf16_rne_df(yh, yl);
-            }
-            o[t] = half[0] | (half[1] << 16);
-          }
+          const uint32_t xu[4] = {xq.x, xq.y, xq.z, xq.w};
+          const float wf[8] = {bf16_lo(wq.x), bf16_hi(wq.x), bf16_lo(wq.y), bf16_hi(wq.y),
+                               bf16_lo(wq.z), bf16_hi(wq.z), bf16_lo(wq.w), bf16_hi(wq.w)};
+          o = bf16x8_scaled_rne(xu, wf, rh, rl);
         }
         // 8 consecutive elements starting at a multiple of 8 stay consecutive in every layout
-        *reinterpret_cast<uint4*>(J.out + layout(8 * v)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(J.out + layout(8 * v)) = o;
       }
     } else {
       for (int k = tid; k < n; k += NT) {
         uint16_t o = 0;
         if (J.valid) {
-          const float p = __fmul_rn(bf16_bits_to_f32(J.x[k]), bf16_bits_to_f32(J.w[k]));
-          const float yh = __fmul_rn(p, rh);
-          const float yl = __fmaf_rn(p, rl, __fmaf_rn(p, rh, -yh));
-          o = bf16_rne_df(yh, yl);
+          o = static_cast<uint16_t>(
+              bf16_scaled_rne(__fmul_rn(bf16_bits_to_f32(J.x[k]), bf16_bits_to_f32(J.w[k])), rh, rl));
         }
         J.out[layout(k)] = o;
       }
     }
   }
+}
+
+// Sums of squares of nvec BF16 rows of n elements (n % 8 == 0, rows 16-byte aligned) as
+// double-floats (exact squares, TwoSum), for the batched kernels' norm prologues. Threads
+// 0..NT-1 call it (they synchronise on named barrier `bar`): NT / nvec consecutive threads share
+// a row, each loads kBatch 16-byte vectors at a time (independent loads in flight), and the
+// partials are added in thread order -- the result does not depend on timing. row(j) gives row
+// j (nullptr: a zero row). With kMax it also returns max_k |x_k * w_k| (exact products) for the
+// weight vector w. part / mpart: NT scratch entries; out / mout: nvec results.
+template <int NT, int kBatch, bool kMax, class RowFn>
+__device__ void sumsq_rows(int nvec, int n, RowFn row, const uint16_t* w, DF* part, float* mpart, DF* out,
+                           float* mout, int bar) {
+  const int tid = threadIdx.x;
+  const int tpv = NT / nvec;
+  const int j = tid / tpv, r = tid - j * tpv;
+  const int nv = n >> 3;
+  DF acc{0.0f, 0.0f};
+  float mx = 0.0f;
+  if (j < nvec) {
+    const uint4* src = reinterpret_cast<const uint4*>(row(j));
+    const uint4* wv = reinterpret_cast<const uint4*>(w);
+    if (src != nullptr) {
+      for (int v0 = r; v0 < nv; v0 += kBatch * tpv) {
+        uint4 q[kBatch], wq[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int v = v0 + i * tpv;
+          q[i] = v < nv ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+          if constexpr (kMax) wq[i] = v < nv ? wv[v] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const uint32_t u[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float lo = bf16_lo(u[t]), hi = bf16_hi(u[t]);
+            df_add(acc, __fmul_rn(lo, lo));
+            df_add(acc, __fmul_rn(hi, hi));
+          }
+          if constexpr (kMax) {
+            const uint32_t wu[4] = {wq[i].x, wq[i].y, wq[i].z, wq[i].w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              mx = fmaxf(mx, fabsf(__fmul_rn(bf16_lo(u[t]), bf16_lo(wu[t]))));
+              mx = fmaxf(mx, fabsf(__fmul_rn(bf16_hi(u[t]), bf16_hi(wu[t]))));
+            }
+          }
+        }
+      }
+    }
+  }
+  part[tid] = acc;
+  if constexpr (kMax) mpart[tid] = mx;
+  asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(NT) : "memory");
+  if (tid < nvec) {
+    DF tot = part[tid * tpv];
+    float m = kMax ? mpart[tid * tpv] : 0.0f;
+    for (int i = 1; i < tpv; ++i) {
+      tot = df_add(tot, part[tid * tpv + i]);
+      if constexpr (kMax) m = fmaxf(m, mpart[tid * tpv + i]);
+    }
+    out[tid] = tot;
+    if constexpr (kMax) mout[tid] = m;
+  }
+  asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(NT) : "memory");
 }
 
 // Shared-memory index of element k of a vector when weight vectors hold 16 elements (FP8) and

@@ -18,6 +18,19 @@ bool g_have[kMaxDevices] = {};
 std::set<std::pair<int, const void*>> g_smem_set;  // (device, kernel) with max smem raised
 }  // namespace
 
+TmapEncodeFn tensor_map_encoder() {
+  static std::once_flag once;
+  static TmapEncodeFn fn = nullptr;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<TmapEncodeFn>(p);
+  });
+  return fn;
+}
+
 cudaError_t device_info(DeviceInfo* info) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);

@@ -249,6 +249,11 @@ cudaError_t launch_input_stage(const InputArgs& in, cudaStream_t stream) {
   const int K = 2 * a.H;
   const size_t misc = kRedBytes + 256;
   const bool rows16 = (K % 8) == 0;
+  if (a.B >= MTP_TC_MIN_B) {
+    bool launched = false;
+    err = launch_input_tc(a, stream, &launched);
+    if (launched || err != cudaSuccess) return err;
+  }
   if (rows16 && a.B <= kTmaMaxB) {
     // the widest warp count whose stages fit next to the concat of B sequences
     const int vec_elems = ((K / 8 + 31) / 32) * 32 * 8;

@@ -1,6 +1,7 @@
 // Host-side declarations shared by the translation units of libmtphead.so.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched through the runtime)
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -22,6 +23,9 @@ namespace mtp {
 #endif
 #ifndef MTP_REGX
 #define MTP_REGX 1
+#endif
+#ifndef MTP_TC_MIN_B
+#define MTP_TC_MIN_B 2  // smallest batch the tensor-core output stage takes
 #endif
 
 constexpr int kWarps = MTP_WARPS;
@@ -46,6 +50,13 @@ cudaError_t device_info(DeviceInfo* info);
 // dynamic shared memory limit once per device. device_info() must have been called first.
 cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        void** args);
+
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry point (so the
+// library does not link against libcuda); nullptr if the driver does not provide it.
+using TmapEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+TmapEncodeFn tensor_map_encoder();
 
 struct InputArgs {
   const uint16_t* embed;
@@ -78,7 +89,13 @@ struct SweepArgs {
 };
 
 cudaError_t launch_input_stage(const InputArgs& a, cudaStream_t stream);
+// Batched (2 <= B <= 16) input stage on tensor cores; *launched stays false when the shape is
+// not supported (H not a multiple of 8, not enough shared memory).
+cudaError_t launch_input_tc(const InputArgs& a, cudaStream_t stream, bool* launched);
 cudaError_t launch_sweep(const SweepArgs& a, cudaStream_t stream);
+// Batched (2 <= B <= 16) output stage on tensor cores; *launched stays false when the shape is
+// not supported (H not a multiple of 8, no tensor-map encoder, not enough shared memory).
+cudaError_t launch_sweep_tc(const SweepArgs& a, cudaStream_t stream, bool* launched);
 cudaError_t launch_quantize(const uint16_t* w, uint8_t* q, float* scale, int32_t* status,
                             int V, int H, cudaStream_t stream);
 

@@ -686,6 +686,11 @@ cudaError_t launch_sweep(const SweepArgs& in, cudaStream_t stream) {
                                     : try_launch_regx<MTP_W_FP8_E4M3>(a, di, grid, stream, &launched);
     if (launched || err != cudaSuccess) return err;
   }
+  if (a.B >= MTP_TC_MIN_B) {
+    bool launched = false;
+    err = launch_sweep_tc(a, stream, &launched);
+    if (launched || err != cudaSuccess) return err;
+  }
   if (rows16 && a.B <= kTmaMaxB) {
     const int vec_elems = ((a.H / EPV + 31) / 32) * 32 * EPV;
     const size_t fixed = static_cast<size_t>(a.B) * vec_elems * 2 + kMisc;

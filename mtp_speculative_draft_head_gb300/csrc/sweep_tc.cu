@@ -1,0 +1,466 @@
+// Batched output stage on tensor cores: B = 2..16 sequences share one pass over lm_head
+// ("glm5next_mtp_head.rs", `forward_one`: shared_head.norm, the lm_head gemv, argmax; here for a
+// batch, as one skinny GEMM  logits[B, V] = xhat[B, H] . lm_head[V, H]^T  fused with the argmax).
+//
+// Why tensor cores here and not at B = 1: per weight byte the batch needs B multiply-adds, which
+// past B ~ 2-4 outruns the fp32 FMA issue rate while HBM still has bandwidth to spare. The need is
+// modest (a 16-sequence BF16 sweep at the HBM roofline is ~110 TFLOP/s, FP8 ~220), so warp-level
+// mma.sync (m16n8k16, FP32 accumulation) covers it with register operands -- which lets FP8 codes
+// be widened straight into A fragments by the hardware E4M3 -> f16 conversion, with no trip
+// through shared memory.
+//
+// Roles (416 threads):
+//  * producer warp: streams 128-row x 128-byte tiles of lm_head with 2-D TMA tensor loads
+//    (128-byte swizzle) into a 12-stage ring (mbarrier full/empty pairs, bounded waits);
+//  * 4 builder warps: compute xhat = rms_norm_vanilla(x, final_norm_w) one k-block at a time
+//    (BF16 for a BF16 head; for FP8, f16 scaled by 2^k per sequence, exact) into a small ring, in
+//    the same swizzled layout, with the same exact rounding as the other kernels;
+//  * 8 consumer warps: 16 rows each of a 128-row tile; ldmatrix + mma.sync, batch as N (8 or 16).
+// Loop order: groups of up to 8 row tiles; per k-block the activations are built once and used by
+// every tile of the group, whose accumulators stay in registers. Each lm_head byte is read once.
+// FP8 A fragments come out of ldmatrix with four codes per register; with k permuted the same way
+// in the activations (codes 4t..4t+3 of a 16-code block sit in k slots 2t, 2t+1, 2t+8, 2t+9 of
+// thread t) every product pairs the right code with the right activation.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace mtp {
+
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kBuilderWarps = 4;
+constexpr int kTcWarps = kConsumerWarps + kBuilderWarps + 1;
+constexpr int kTcThreads = kTcWarps * 32;          // 416
+constexpr int kPrologueThreads = (kConsumerWarps + kBuilderWarps) * 32;  // 384
+constexpr int kTileRows = 16 * kConsumerWarps;     // 128
+constexpr int kTileGroup = 8;
+constexpr int kATileBytes = kTileRows * 128;       // 16 KB: 128 rows x 128 bytes
+constexpr int kAStages = 12;
+constexpr int kBStages = 4;
+constexpr int kSeq = 16;                           // activation rows per B tile (N <= 16)
+constexpr int kProducerWarp = kConsumerWarps + kBuilderWarps;
+
+template <int WT>
+struct TcCfg {
+  static constexpr int kKbElems = (WT == MTP_W_BF16) ? 64 : 128;  // weights per row per k-block
+  static constexpr int kBTileBytes = kSeq * kKbElems * 2;         // bf16 / f16 activations
+};
+
+// ---------------------------------------------------------------------------- MMA of one stage
+// BF16 head: A = 128 rows x 64 k (this warp's 16 rows), B = 16 sequences x 64 k.
+template <int NT>
+__device__ __forceinline__ void stage_mma_bf16(uint32_t a_base, uint32_t b_base, float (&acc)[NT][4],
+                                               int warp, int lane) {
+  const int ar = 16 * warp + (lane & 15);
+  const int bn = (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    uint32_t a[4];
+    ldmatrix_x4(a, a_base + swz(ar, 2 * kk + (lane >> 4)));
+    if constexpr (NT == 2) {
+      uint32_t b[4];
+      ldmatrix_x4(b, b_base + swz(bn, 2 * kk + ((lane >> 3) & 1)));
+      mma_bf16(acc[0], a, b[0], b[1]);
+      mma_bf16(acc[1], a, b[2], b[3]);
+    } else {
+      uint32_t b[2];
+      ldmatrix_x2(b, b_base + swz(lane & 7, 2 * kk + ((lane >> 3) & 1)));
+      mma_bf16(acc[0], a, b[0], b[1]);
+    }
+  }
+}
+
+// FP8 head: A = 128 rows x 128 codes, B = 16 sequences x 128 f16 (two 64-element sub-tiles).
+template <int NT>
+__device__ __forceinline__ void stage_mma_fp8(uint32_t a_base, uint32_t b_base, float (&acc)[NT][4],
+                                              int warp, int lane) {
+  const int ar = 16 * warp + (lane & 15);
+  const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t r[4];
+    ldmatrix_x4(r, a_base + swz(ar, 2 * q + (lane >> 4)));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t a[4];
+      e4m3x4_to_f16x2x2(r[2 * h], a[0], a[2]);      // row g:   codes 4t4, 4t4+1 | 4t4+2, 4t4+3
+      e4m3x4_to_f16x2x2(r[2 * h + 1], a[1], a[3]);  // row g+8
+      const int kin = 32 * q + 16 * h + 4 * t4;     // code offset within the 128-code block
+      const int st = kin >> 6, ke = kin & 63;
+#pragma unroll
+      for (int jn = 0; jn < NT; ++jn) {
+        const int n = 8 * jn + g;
+        uint32_t b0, b1;
+        lds_v2(b0, b1, b_base + st * 2048 + swz(n, ke >> 3) + ((ke & 7) << 1));
+        mma_f16(acc[jn], a, b0, b1);
+      }
+    }
+  }
+}
+
+// CTA combine of per-warp bests (wbest[warp * kSeq + b]) and the last-CTA-done grid argmax.
+__device__ void tc_argmax_finish(int nb, const ArgBest* wbest, uint8_t* ws, int32_t* draft) {
+  __shared__ int is_last;
+  ArgBest* part = reinterpret_cast<ArgBest*>(ws + kWsHeader);
+  unsigned int* counter = reinterpret_cast<unsigned int*>(ws);
+  if (threadIdx.x < nb) {
+    ArgBest c{0.0f, -1};
+    for (int w = 0; w < kTcWarps; ++w) {
+      const ArgBest o = wbest[w * kSeq + threadIdx.x];
+      if (o.i >= 0) arg_update(c, o.v, o.i);
+    }
+    part[blockIdx.x * nb + threadIdx.x] = c;
+    __threadfence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = (atomicAdd(counter, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (is_last) {
+    __threadfence();
+    if (threadIdx.x < nb) {
+      ArgBest c{0.0f, -1};
+      for (unsigned int gi = 0; gi < gridDim.x; ++gi) {
+        const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(part + gi * nb + threadIdx.x));
+        const ArgBest o{__uint_as_float(raw.x), static_cast<int32_t>(raw.y)};
+        if (o.i >= 0) arg_update(c, o.v, o.i);
+      }
+      draft[threadIdx.x] = c.i;
+    }
+    if (threadIdx.x == 0) atomicExch(counter, 0u);
+  }
+}
+
+// ---------------------------------------------------------------------------- the kernel
+template <int WT, int NT>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    sweep_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const SweepArgs a) {
+  using Cfg = TcCfg<WT>;
+  constexpr int KBE = Cfg::kKbElems;
+  constexpr int BTB = Cfg::kBTileBytes;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle pattern
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* aring = smem;
+  uint8_t* bring = aring + kAStages * kATileBytes;
+  uint64_t* afull = reinterpret_cast<uint64_t*>(bring + kBStages * BTB);
+  uint64_t* aempty = afull + kAStages;
+  uint64_t* bfull = aempty + kAStages;
+  uint64_t* bempty = bfull + kBStages;
+  float* nrm = reinterpret_cast<float*>(bempty + kBStages);  // rh, rl, xscale, unscale [4][16]
+  ArgBest* wbest = reinterpret_cast<ArgBest*>(nrm + 4 * kSeq);
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int B = a.B, H = a.H;
+  const int64_t V = a.V;
+  const int KB = (H + KBE - 1) / KBE;
+  const int T = static_cast<int>((V + kTileRows - 1) / kTileRows);
+  const int t0 = static_cast<int>(static_cast<int64_t>(T) * blockIdx.x / gridDim.x);
+  const int t1 = static_cast<int>(static_cast<int64_t>(T) * (blockIdx.x + 1) / gridDim.x);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(smem_addr(&afull[i]), 1);
+      mbar_init(smem_addr(&aempty[i]), kConsumerWarps);
+    }
+    for (int i = 0; i < kBStages; ++i) {
+      mbar_init(smem_addr(&bfull[i]), kBuilderWarps);
+      mbar_init(smem_addr(&bempty[i]), kConsumerWarps);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  for (int i = threadIdx.x; i < kTcWarps * kSeq; i += kTcThreads) wbest[i] = ArgBest{0.0f, -1};
+  __syncthreads();
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------------ producer
+    int issued = 0;
+    if (lane == 0) {
+      const uint64_t policy = l2_evict_first_policy();
+      int slot = 0;
+      uint32_t ep = 1;
+      bool ok = true;
+      for (int gt = t0; gt < t1 && ok; gt += kTileGroup) {
+        const int ntile = (t1 - gt) < kTileGroup ? (t1 - gt) : kTileGroup;
+        for (int kb = 0; kb < KB && ok; ++kb) {
+          for (int j = 0; j < ntile; ++j) {
+            if (*reinterpret_cast<volatile int*>(&abort_flag) || !mbar_wait_bounded(smem_addr(&aempty[slot]), ep)) {
+              ok = false;
+              break;
+            }
+            const uint32_t bar = smem_addr(&afull[slot]);
+            mbar_arrive_expect_tx(bar, kATileBytes);
+            tma_load_2d(smem_addr(aring + slot * kATileBytes), &tmap_w, kb * KBE, (gt + j) * kTileRows, bar,
+                        policy);
+            ++issued;
+            if (++slot == kAStages) { slot = 0; ep ^= 1u; }
+          }
+        }
+      }
+      if (!ok) {
+        store_status(a.status, MTP_ERR_TIMEOUT);
+        atomicExch(&abort_flag, 1);
+      }
+      // every copy issued must land before the CTA's shared memory goes away
+      for (int s = 0; s < kAStages && s < issued; ++s) {
+        const int uses = (issued - s + kAStages - 1) / kAStages;
+        (void)mbar_wait_bounded(smem_addr(&afull[s]), static_cast<uint32_t>((uses - 1) & 1));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ prologue (warps 0..11)
+    pdl_wait_prior_grid();  // x comes from the preceding kernel
+    {
+      // the activation ring is free until the builders start: scratch of the sums of squares
+      DF* part = reinterpret_cast<DF*>(bring);
+      float* mpart = reinterpret_cast<float*>(part + kPrologueThreads);
+      DF* tot = reinterpret_cast<DF*>(mpart + kPrologueThreads);
+      float* mtot = reinterpret_cast<float*>(tot + kSeq);
+      auto row = [&](int b) -> const uint16_t* { return a.x + static_cast<size_t>(b) * H; };
+      sumsq_rows<kPrologueThreads, 8, WT == MTP_W_FP8_E4M3>(B, H, row, a.final_norm_w, part, mpart, tot, mtot, 1);
+      if (threadIdx.x < B) {
+        const int b = threadIdx.x;
+        const double ms = (static_cast<double>(tot[b].hi) + static_cast<double>(tot[b].lo)) / static_cast<double>(H);
+        const double rr = 1.0 / sqrt(ms + static_cast<double>(a.eps));
+        const float rh = static_cast<float>(rr);
+        const float rl = static_cast<float>(rr - static_cast<double>(rh));
+        nrm[b] = rh;
+        nrm[kSeq + b] = rl;
+        float xs = 1.0f, us = 1.0f;
+        if constexpr (WT == MTP_W_FP8_E4M3) {
+          // largest |xhat| of this sequence: rounding is monotonic, so it is the rounded max
+          const float mx = mtot[b];
+          const float yh = __fmul_rn(mx, rh);
+          const float yl = __fmaf_rn(mx, rl, __fmaf_rn(mx, rh, -yh));
+          const float m = bf16_bits_to_f32(bf16_rne_df(yh, yl));
+          if (m > 0.0f && m <= 3.0e38f) {
+            int e = 0;
+            (void)frexpf(m, &e);
+            xs = ldexpf(1.0f, 15 - e);
+            us = ldexpf(1.0f, e - 15);
+          }
+        }
+        nrm[2 * kSeq + b] = xs;
+        nrm[3 * kSeq + b] = us;
+      }
+    }
+    named_barrier_sync(1, kPrologueThreads);
+    pdl_launch_dependents();
+
+    if (warp >= kConsumerWarps) {
+      // ---------------------------------------------------------------- builders
+      const int bt = threadIdx.x - kConsumerWarps * 32;  // 0..127
+      const int n = bt >> 3, c = bt & 7;
+      const bool live = n < B;
+      const float rh = live ? nrm[n] : 0.0f, rl = live ? nrm[kSeq + n] : 0.0f;
+      const float xs = live ? nrm[2 * kSeq + n] : 1.0f;
+      const uint16_t* xrow = a.x + static_cast<size_t>(live ? n : 0) * H;
+      int slot = 0;
+      uint32_t ep = 1;
+      for (int gt = t0; gt < t1; gt += kTileGroup) {
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (*reinterpret_cast<volatile int*>(&abort_flag) ||
+              !__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&bempty[slot]), ep))) {
+            ok = false;
+            break;
+          }
+          uint8_t* bt_base = bring + slot * BTB;
+#pragma unroll
+          for (int sub = 0; sub < BTB / 2048; ++sub) {
+            const int k0 = kb * KBE + 64 * sub + 8 * c;
+            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+            if (live && k0 < H) {
+              const uint4 xq = *reinterpret_cast<const uint4*>(xrow + k0);
+              const uint4 wq = *reinterpret_cast<const uint4*>(a.final_norm_w + k0);
+              const uint32_t xu[4] = {xq.x, xq.y, xq.z, xq.w};
+              const float wf[8] = {bf16_lo(wq.x), bf16_hi(wq.x), bf16_lo(wq.y), bf16_hi(wq.y),
+                                   bf16_lo(wq.z), bf16_hi(wq.z), bf16_lo(wq.w), bf16_hi(wq.w)};
+              o = bf16x8_scaled_rne(xu, wf, rh, rl);  // xhat, BF16
+              if constexpr (WT == MTP_W_FP8_E4M3) {
+                // f16 of xhat * 2^k (exact inside the f16 range)
+                uint32_t* ov = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                  ov[t] = f16_bits(__fmul_rn(bf16_lo(ov[t]), xs)) | (f16_bits(__fmul_rn(bf16_hi(ov[t]), xs)) << 16);
+              }
+            }
+            *reinterpret_cast<uint4*>(bt_base + sub * 2048 + swz(n, c)) = o;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&bfull[slot]));
+          if (++slot == kBStages) { slot = 0; ep ^= 1u; }
+        }
+        if (!ok) {
+          if (lane == 0) {
+            store_status(a.status, MTP_ERR_TIMEOUT);
+            atomicExch(&abort_flag, 1);
+          }
+          break;
+        }
+      }
+    } else {
+      // ---------------------------------------------------------------- consumers
+      const int g = lane >> 2, t4 = lane & 3;
+      ArgBest best[NT][2];
+#pragma unroll
+      for (int jn = 0; jn < NT; ++jn) best[jn][0] = best[jn][1] = ArgBest{0.0f, -1};
+      int aslot = 0, bslot = 0;
+      uint32_t ap = 0, bp = 0;
+      bool ok = true;
+      for (int gt = t0; gt < t1 && ok; gt += kTileGroup) {
+        const int ntile = (t1 - gt) < kTileGroup ? (t1 - gt) : kTileGroup;
+        float acc[kTileGroup][NT][4];
+#pragma unroll
+        for (int j = 0; j < kTileGroup; ++j)
+#pragma unroll
+          for (int jn = 0; jn < NT; ++jn) acc[j][jn][0] = acc[j][jn][1] = acc[j][jn][2] = acc[j][jn][3] = 0.0f;
+        // row scales of the FP8 head for this thread's rows, loaded ahead of the epilogue
+        float scl[kTileGroup][2];
+#pragma unroll
+        for (int j = 0; j < kTileGroup; ++j) {
+          scl[j][0] = scl[j][1] = 1.0f;
+          if constexpr (WT == MTP_W_FP8_E4M3) {
+            const int64_t r0 = static_cast<int64_t>(gt + j) * kTileRows + 16 * warp + g;
+            if (j < ntile && r0 < V) scl[j][0] = __ldg(a.scale + r0);
+            if (j < ntile && r0 + 8 < V) scl[j][1] = __ldg(a.scale + r0 + 8);
+          }
+        }
+        for (int kb = 0; kb < KB && ok; ++kb) {
+          if (*reinterpret_cast<volatile int*>(&abort_flag) ||
+              !__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&bfull[bslot]), bp))) {
+            ok = false;
+            break;
+          }
+          const uint32_t b_base = smem_addr(bring + bslot * BTB);
+#pragma unroll
+          for (int j = 0; j < kTileGroup; ++j) {
+            if (j < ntile && ok) {
+              if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&afull[aslot]), ap))) {
+                ok = false;
+              } else {
+                const uint32_t a_base = smem_addr(aring + aslot * kATileBytes);
+                if constexpr (WT == MTP_W_BF16) stage_mma_bf16<NT>(a_base, b_base, acc[j], warp, lane);
+                else stage_mma_fp8<NT>(a_base, b_base, acc[j], warp, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&aempty[aslot]));
+                if (++aslot == kAStages) { aslot = 0; ap ^= 1u; }
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&bempty[bslot]));
+          if (++bslot == kBStages) { bslot = 0; bp ^= 1u; }
+        }
+        if (!ok) break;
+        // epilogue of the group: logits and per-sequence running argmax
+#pragma unroll
+        for (int j = 0; j < kTileGroup; ++j) {
+          if (j < ntile) {
+            const int64_t rbase = static_cast<int64_t>(gt + j) * kTileRows + 16 * warp + g;
+#pragma unroll
+            for (int jn = 0; jn < NT; ++jn) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int n = 8 * jn + 2 * t4 + (i & 1);
+                const int64_t row = rbase + 8 * (i >> 1);
+                if (n < B && row < V) {
+                  float v = acc[j][jn][i];
+                  if constexpr (WT == MTP_W_FP8_E4M3) v = __fmul_rn(__fmul_rn(v, nrm[3 * kSeq + n]), scl[j][i >> 1]);
+                  if (a.logits != nullptr) a.logits[static_cast<int64_t>(n) * V + row] = v;
+                  arg_update(best[jn][i & 1], v, static_cast<int32_t>(row));
+                }
+              }
+            }
+          }
+        }
+      }
+      if (!ok && lane == 0) {
+        store_status(a.status, MTP_ERR_TIMEOUT);
+        atomicExch(&abort_flag, 1);
+      }
+      // combine lanes that hold the same sequences (same t4), then publish per warp
+#pragma unroll
+      for (int jn = 0; jn < NT; ++jn)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          ArgBest b = best[jn][hh];
+#pragma unroll
+          for (int m = 4; m < 32; m <<= 1) {
+            const float v = __shfl_xor_sync(0xffffffffu, b.v, m);
+            const int32_t i = __shfl_xor_sync(0xffffffffu, b.i, m);
+            if (i >= 0) arg_update(b, v, i);
+          }
+          const int n = 8 * jn + 2 * t4 + hh;
+          if (g == 0 && n < B) wbest[warp * kSeq + n] = b;
+        }
+    }
+  }
+  __syncthreads();
+  pdl_wait_prior_grid();  // the workspace may still be read by the kernel before (no-op if done)
+  tc_argmax_finish(B, wbest, a.ws, a.draft);
+}
+
+// ---------------------------------------------------------------------------- host side
+template <int WT, int NT>
+cudaError_t launch_tc(const SweepArgs& a, const CUtensorMap& tm, unsigned grid, size_t smem, cudaStream_t stream) {
+  SweepArgs args = a;
+  CUtensorMap tmc = tm;
+  void* params[] = {&tmc, &args};
+  return launch_pdl(reinterpret_cast<const void*>(sweep_tc_kernel<WT, NT>), dim3(grid), dim3(kTcThreads), smem,
+                    stream, params);
+}
+
+}  // namespace
+
+size_t sweep_tc_smem_bytes(int w_dtype) {
+  const int btb = (w_dtype == MTP_W_BF16) ? TcCfg<MTP_W_BF16>::kBTileBytes : TcCfg<MTP_W_FP8_E4M3>::kBTileBytes;
+  return 1024 + static_cast<size_t>(kAStages) * kATileBytes + static_cast<size_t>(kBStages) * btb +
+         (2 * kAStages + 2 * kBStages) * 8 + 4 * kSeq * 4 + kTcWarps * kSeq * sizeof(ArgBest) + 64;
+}
+
+cudaError_t launch_sweep_tc(const SweepArgs& a, cudaStream_t stream, bool* launched) {
+  *launched = false;
+  const int EB = (a.w_dtype == MTP_W_BF16) ? 2 : 1;
+  if (a.B < 2 || a.B > kSeq) return cudaSuccess;
+  if ((static_cast<int64_t>(a.H) * EB) % 16 != 0 || (a.H % 8) != 0) return cudaSuccess;
+  DeviceInfo di;
+  cudaError_t err = device_info(&di);
+  if (err != cudaSuccess) return err;
+  const size_t smem = sweep_tc_smem_bytes(a.w_dtype);
+  if (smem > static_cast<size_t>(di.smem_optin)) return cudaSuccess;
+  const TmapEncodeFn enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaSuccess;
+  CUtensorMap tm;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.H), static_cast<cuuint64_t>(a.V)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.H) * EB};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(a.w_dtype == MTP_W_BF16 ? 64 : 128),
+                             static_cast<cuuint32_t>(kTileRows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult cr = enc(&tm, a.w_dtype == MTP_W_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                          2, const_cast<uint8_t*>(a.W), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaSuccess;
+  const int64_t T = (static_cast<int64_t>(a.V) + kTileRows - 1) / kTileRows;
+  int64_t g = di.sm_count < T ? di.sm_count : T;
+  if (g > kMaxGrid) g = kMaxGrid;
+  const unsigned grid = static_cast<unsigned>(g < 1 ? 1 : g);
+  *launched = true;
+  if (a.w_dtype == MTP_W_BF16)
+    return a.B <= 8 ? launch_tc<MTP_W_BF16, 1>(a, tm, grid, smem, stream) : launch_tc<MTP_W_BF16, 2>(a, tm, grid, smem, stream);
+  return a.B <= 8 ? launch_tc<MTP_W_FP8_E4M3, 1>(a, tm, grid, smem, stream)
+                  : launch_tc<MTP_W_FP8_E4M3, 2>(a, tm, grid, smem, stream);
+}
+
+}  // namespace mtp

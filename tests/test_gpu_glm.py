@@ -11,7 +11,7 @@ import torch
 import mtp_speculative_draft_head_gb300 as m
 import oracle
 import synth
-from gpu_helpers import TOL_BF16, TOL_FP8, check_draft, check_logits_and_draft, check_x
+from gpu_helpers import TOL_BF16, TOL_FP8, abs_product_sums, check_draft, check_logits_and_draft, check_x
 
 pytestmark = pytest.mark.gpu
 
@@ -40,9 +40,12 @@ class Model:
         self.sb = self.head.row_scale.cpu().numpy()
 
     def oracle_x(self, tokens, hidden):
-        return oracle.input_stage(self.wb["embed"], self.wb["enorm_w"], self.wb["hnorm_w"],
-                                  self.wb["eh_proj"], _bits(tokens).astype(np.int64), _bits(hidden), EPS,
-                                  return_sums=True)
+        """(x, status, sums, band sums): the last is None for one sequence (error-free sum)."""
+        x, concat, st, sums = oracle.input_stage(self.wb["embed"], self.wb["enorm_w"], self.wb["hnorm_w"],
+                                                 self.wb["eh_proj"], _bits(tokens).astype(np.int64), _bits(hidden),
+                                                 EPS, return_concat=True, return_sums=True)
+        abs_sums = abs_product_sums(self.wb["eh_proj"], concat) if x.shape[0] >= 2 else None
+        return x, st, sums, abs_sums
 
     def oracle_logits(self, x_bits, fp8):
         xhat = oracle.final_norm(x_bits, self.wb["final_norm_w"], EPS)
@@ -78,9 +81,11 @@ def test_glm_head(glm, B, fp8):
     x, logits, draft = glm.head.forward(tokens, hidden, fp8=fp8, logits=True, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    x_ref, st, sums = glm.oracle_x(tokens, hidden)
+    x_ref, st, sums, abs_sums = glm.oracle_x(tokens, hidden)
     assert np.all(st == 0)
-    check_x(_bits(x), x_ref, sums)
+    n_diff = check_x(_bits(x), x_ref, sums, abs_sums)
+    # the band is a worst-case bound; the FP32 runs differ from the exact sum far more rarely
+    assert n_diff <= max(1, x_ref.size // 100)
     ref = glm.oracle_logits(x_ref, fp8)
     err = check_logits_and_draft(logits.cpu().numpy(), draft.cpu().numpy(), ref, TOL_FP8 if fp8 else TOL_BF16)
     assert err < 5e-3
@@ -107,7 +112,7 @@ def test_adversarial_ties_and_outliers():
     md = Model(H, V, seed, outliers=True)
     tokens, hidden = synth.make_step_inputs(H, V, 1, seed, DEV)
     hidden = synth.hidden_with_outlier_channels(hidden, 5, 100.0, seed)
-    x_ref, _, sums = md.oracle_x(tokens, hidden)
+    x_ref, _, sums, _ = md.oracle_x(tokens, hidden)
     xhat = oracle.final_norm(x_ref, md.wb["final_norm_w"], EPS)[0]
     rows = synth.pick_rows(V, 64, seed, DEV)
     md.w.lm_head = synth.plant_rows(md.w.lm_head, rows, torch.from_numpy(oracle.bf16_to_f64(xhat)))

@@ -1,6 +1,8 @@
 """GPU parity of the CUDA library (through its C ABI) against the CPU oracle on small and
 medium shapes: several tiles and ragged tails, both weight dtypes, every kernel path
-(bulk-copy pipelines for 16-byte rows and B <= 4, plain-load kernels otherwise), plus the
+(register-xhat and bulk-copy pipelines for B = 1; for B >= 2 the tensor-core kernels -- output
+stage when H is a multiple of 8, input stage when H is a multiple of 32 -- and plain-load
+kernels otherwise), plus the
 edge cases: out-of-range tokens, NaN/Inf, exact ties, determinism, CUDA-graph replay and the
 quantiser bit for bit."""
 import numpy as np
@@ -10,7 +12,8 @@ import torch
 import mtp_speculative_draft_head_gb300 as m
 import oracle
 import synth
-from gpu_helpers import TOL_BF16, TOL_FP8, check_draft, check_logits_and_draft, check_x, lowest_argmax
+from gpu_helpers import (TOL_BF16, TOL_FP8, abs_product_sums, check_draft, check_logits_and_draft, check_x,
+                         lowest_argmax)
 
 pytestmark = pytest.mark.gpu
 
@@ -60,9 +63,14 @@ class Case:
         return logits, draft, int(st.item())
 
     def oracle_input(self):
-        return oracle.input_stage(self.wb["embed"], self.wb["enorm_w"], self.wb["hnorm_w"], self.wb["eh_proj"],
-                                  _bits(self.tokens).astype(np.int64), _bits(self.hidden), EPS,
-                                  return_sums=True)
+        x, self.concat_ref, st, sums = oracle.input_stage(
+            self.wb["embed"], self.wb["enorm_w"], self.wb["hnorm_w"], self.wb["eh_proj"],
+            _bits(self.tokens).astype(np.int64), _bits(self.hidden), EPS, return_concat=True, return_sums=True)
+        return x, st, sums
+
+    def abs_sums(self):
+        """Band of the batched input stage (None for one sequence: error-free sum)."""
+        return abs_product_sums(self.wb["eh_proj"], self.concat_ref) if self.B >= 2 else None
 
     def oracle_logits(self, x_bits, wt, W_bits, scale):
         xhat = oracle.final_norm(x_bits, self.wb["final_norm_w"], EPS)
@@ -72,13 +80,19 @@ class Case:
 SHAPES = [  # (H, V, B): tiles, ragged tails and every path
     (256, 4096, 1),     # the small workload
     (1000, 5003, 1),    # BF16 rows of 2000 B (one partial chunk); FP8 rows not 16-B -> plain path
-    (1000, 5003, 3),
-    (2056, 1031, 2),    # BF16 rows of 4112 B: a full chunk and a 16-byte tail chunk
-    (2048, 777, 4),     # FP8 rows of 2048 B on the bulk-copy path, B = 4
+    (1000, 5003, 3),    # B >= 2, H % 8 == 0 -> tensor-core kernel (partial last k-block)
+    (2056, 1031, 2),    # tensor-core kernel, ragged last row tile
+    (2048, 777, 4),
     (6144, 1000, 1),    # GLM hidden size: 3 BF16 chunks, FP8 one full + one partial chunk
-    (4096, 300, 5),     # B = 5 -> plain kernels
-    (512, 2000, 16),    # B = 16 -> plain kernels
-    (100, 50, 2),       # odd H -> plain kernels
+    (4096, 300, 5),
+    (512, 2000, 16),    # B = 16: two n-tiles of 8 sequences
+    (544, 160000, 9),   # output: more than 8 row tiles per CTA; input: a k-chunk across the
+                        # embedding / hidden boundary and a partial last chunk
+    (6144, 3000, 16),
+    (96, 300, 3),       # input: one partial k-chunk holding both halves
+    (16384, 1000, 2),   # input: more 8-row groups than 8 per SM -> more CTAs than SMs
+    (8, 300, 2),        # output: a single, partial k-block; input: H % 32 != 0 -> error-free kernel
+    (100, 50, 2),       # H % 8 != 0 -> plain kernels
     (8, 7, 1),
     (64, 1, 1),         # V = 1
 ]
@@ -92,7 +106,7 @@ def test_head_matches_oracle(H, V, B, fp8):
     assert np.all(st_ref == 0)
     x_gpu, st = c.input_gpu()
     assert st == 0
-    check_x(_bits(x_gpu), x_ref, sums)
+    check_x(_bits(x_gpu), x_ref, sums, c.abs_sums())
     if fp8:
         q, s, qst = c.quantize_gpu()
         assert qst == 0
@@ -171,9 +185,10 @@ def test_out_of_range_tokens_flag_and_zero_rows():
     x, st = c.input_gpu(tokens=tokens)
     assert st == m.ERR_TOKEN_RANGE
     assert torch.all(x[1:] == 0)
-    x_ref, _, sums = oracle.input_stage(c.wb["embed"], c.wb["enorm_w"], c.wb["hnorm_w"], c.wb["eh_proj"],
-                                        [11, c.V + 3, -1], _bits(c.hidden), EPS, return_sums=True)
-    check_x(_bits(x), x_ref, sums)
+    x_ref, concat, _, sums = oracle.input_stage(c.wb["embed"], c.wb["enorm_w"], c.wb["hnorm_w"], c.wb["eh_proj"],
+                                                [11, c.V + 3, -1], _bits(c.hidden), EPS, return_concat=True,
+                                                return_sums=True)
+    check_x(_bits(x), x_ref, sums, abs_product_sums(c.wb["eh_proj"], concat))
     # a zero x gives all-zero logits: every logit ties and index 0 wins
     logits, draft, _ = c.output_gpu(x, c.g["lm_head"], None, m.W_BF16)
     assert torch.all(logits[1:] == 0) and draft[1:].tolist() == [0, 0]
