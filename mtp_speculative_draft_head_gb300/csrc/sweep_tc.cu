@@ -39,7 +39,12 @@ constexpr int kTcWarps = kConsumerWarps + kBuilderWarps + 1;
 constexpr int kTcThreads = kTcWarps * 32;          // 416
 constexpr int kPrologueThreads = (kConsumerWarps + kBuilderWarps) * 32;  // 384
 constexpr int kTileRows = 16 * kConsumerWarps;     // 128
-constexpr int kTileGroup = 8;
+// Row tiles per group (their accumulators stay in registers while the activations of a k-block
+// are reused across them). 13 warps put 4 on one SM sub-partition, so a thread has at most 128
+// registers: the FP8 head with 16 sequences (two n-tiles, 32 registers of activation fragments)
+// takes groups of 4.
+template <int WT, int NT>
+__host__ __device__ constexpr int tile_group() { return (WT == MTP_W_FP8_E4M3 && NT == 2) ? 4 : 8; }
 constexpr int kATileBytes = kTileRows * 128;       // 16 KB: 128 rows x 128 bytes
 constexpr int kAStages = 12;
 constexpr int kBStages = 4;
@@ -53,56 +58,78 @@ struct TcCfg {
 };
 
 // ---------------------------------------------------------------------------- MMA of one stage
-// BF16 head: A = 128 rows x 64 k (this warp's 16 rows), B = 16 sequences x 64 k.
-template <int NT>
-__device__ __forceinline__ void stage_mma_bf16(uint32_t a_base, uint32_t b_base, float (&acc)[NT][4],
-                                               int warp, int lane) {
-  const int ar = 16 * warp + (lane & 15);
-  const int bn = (lane & 7) + ((lane >> 4) << 3);
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    uint32_t a[4];
-    ldmatrix_x4(a, a_base + swz(ar, 2 * kk + (lane >> 4)));
-    if constexpr (NT == 2) {
-      uint32_t b[4];
-      ldmatrix_x4(b, b_base + swz(bn, 2 * kk + ((lane >> 3) & 1)));
-      mma_bf16(acc[0], a, b[0], b[1]);
-      mma_bf16(acc[1], a, b[2], b[3]);
-    } else {
-      uint32_t b[2];
-      ldmatrix_x2(b, b_base + swz(lane & 7, 2 * kk + ((lane >> 3) & 1)));
-      mma_bf16(acc[0], a, b[0], b[1]);
-    }
-  }
-}
+// The activation (B-operand) fragments of a k-block are the same for every row tile of a group:
+// they are loaded into registers once per k-block (and the activation stage released at once).
+template <int WT, int NT>
+struct BFrags;
 
-// FP8 head: A = 128 rows x 128 codes, B = 16 sequences x 128 f16 (two 64-element sub-tiles).
+// BF16 head: k-block of 64, four k16-steps; fragment (b0, b1) per step and n-tile.
 template <int NT>
-__device__ __forceinline__ void stage_mma_fp8(uint32_t a_base, uint32_t b_base, float (&acc)[NT][4],
-                                              int warp, int lane) {
-  const int ar = 16 * warp + (lane & 15);
-  const int g = lane >> 2, t4 = lane & 3;
+struct BFrags<MTP_W_BF16, NT> {
+  uint32_t r[4][NT][2];
+  __device__ __forceinline__ void load(uint32_t b_base, int lane) {
+    const int bn = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t r[4];
-    ldmatrix_x4(r, a_base + swz(ar, 2 * q + (lane >> 4)));
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t a[4];
-      e4m3x4_to_f16x2x2(r[2 * h], a[0], a[2]);      // row g:   codes 4t4, 4t4+1 | 4t4+2, 4t4+3
-      e4m3x4_to_f16x2x2(r[2 * h + 1], a[1], a[3]);  // row g+8
-      const int kin = 32 * q + 16 * h + 4 * t4;     // code offset within the 128-code block
-      const int st = kin >> 6, ke = kin & 63;
-#pragma unroll
-      for (int jn = 0; jn < NT; ++jn) {
-        const int n = 8 * jn + g;
-        uint32_t b0, b1;
-        lds_v2(b0, b1, b_base + st * 2048 + swz(n, ke >> 3) + ((ke & 7) << 1));
-        mma_f16(acc[jn], a, b0, b1);
+    for (int kk = 0; kk < 4; ++kk) {
+      if constexpr (NT == 2) {
+        uint32_t b[4];
+        ldmatrix_x4(b, b_base + swz(bn, 2 * kk + ((lane >> 3) & 1)));
+        r[kk][0][0] = b[0]; r[kk][0][1] = b[1]; r[kk][1][0] = b[2]; r[kk][1][1] = b[3];
+      } else {
+        uint32_t b[2];
+        ldmatrix_x2(b, b_base + swz(lane & 7, 2 * kk + ((lane >> 3) & 1)));
+        r[kk][0][0] = b[0]; r[kk][0][1] = b[1];
       }
     }
   }
-}
+  // A = this warp's 16 rows x 64 k of a 128-row tile
+  __device__ __forceinline__ void mma(uint32_t a_base, float (&acc)[NT][4], int warp, int lane) const {
+    const int ar = 16 * warp + (lane & 15);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t a[4];
+      ldmatrix_x4(a, a_base + swz(ar, 2 * kk + (lane >> 4)));
+#pragma unroll
+      for (int jn = 0; jn < NT; ++jn) mma_bf16(acc[jn], a, r[kk][jn][0], r[kk][jn][1]);
+    }
+  }
+};
+
+// FP8 head: k-block of 128 codes, eight k16-steps over two 64-element activation sub-tiles.
+// ldmatrix hands each thread four consecutive codes (4*t4 .. 4*t4+3 of a 16-code block); they
+// fill k slots 2*t4, 2*t4+1, 2*t4+8, 2*t4+9 of the MMA, so the activation fragment of that
+// thread is x[4*t4 .. 4*t4+3] of the same block -- one 8-byte load.
+template <int NT>
+struct BFrags<MTP_W_FP8_E4M3, NT> {
+  uint32_t r[8][NT][2];
+  __device__ __forceinline__ void load(uint32_t b_base, int lane) {
+    const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const int kin = 16 * s + 4 * t4;  // code offset within the 128-code block
+      const int st = kin >> 6, ke = kin & 63;
+#pragma unroll
+      for (int jn = 0; jn < NT; ++jn)
+        lds_v2(r[s][jn][0], r[s][jn][1], b_base + st * 2048 + swz(8 * jn + g, ke >> 3) + ((ke & 7) << 1));
+    }
+  }
+  __device__ __forceinline__ void mma(uint32_t a_base, float (&acc)[NT][4], int warp, int lane) const {
+    const int ar = 16 * warp + (lane & 15);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t c[4];
+      ldmatrix_x4(c, a_base + swz(ar, 2 * q + (lane >> 4)));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t a[4];
+        e4m3x4_to_f16x2x2(c[2 * h], a[0], a[2]);      // row g:   codes 4t4, 4t4+1 | 4t4+2, 4t4+3
+        e4m3x4_to_f16x2x2(c[2 * h + 1], a[1], a[3]);  // row g+8
+#pragma unroll
+        for (int jn = 0; jn < NT; ++jn) mma_f16(acc[jn], a, r[2 * q + h][jn][0], r[2 * q + h][jn][1]);
+      }
+    }
+  }
+};
 
 // CTA combine of per-warp bests (wbest[warp * kSeq + b]) and the last-CTA-done grid argmax.
 __device__ void tc_argmax_finish(int nb, const ArgBest* wbest, uint8_t* ws, int32_t* draft) {
@@ -141,6 +168,7 @@ template <int WT, int NT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     sweep_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const SweepArgs a) {
   using Cfg = TcCfg<WT>;
+  constexpr int kTileGroup = tile_group<WT, NT>();
   constexpr int KBE = Cfg::kKbElems;
   constexpr int BTB = Cfg::kBTileBytes;
   extern __shared__ uint8_t smem_raw[];
@@ -288,10 +316,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               o = bf16x8_scaled_rne(xu, wf, rh, rl);  // xhat, BF16
               if constexpr (WT == MTP_W_FP8_E4M3) {
                 // f16 of xhat * 2^k (exact inside the f16 range)
-                uint32_t* ov = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-                for (int t = 0; t < 4; ++t)
-                  ov[t] = f16_bits(__fmul_rn(bf16_lo(ov[t]), xs)) | (f16_bits(__fmul_rn(bf16_hi(ov[t]), xs)) << 16);
+                auto f16x2 = [xs](uint32_t v) {
+                  return f16_bits(__fmul_rn(bf16_lo(v), xs)) | (f16_bits(__fmul_rn(bf16_hi(v), xs)) << 16);
+                };
+                o = make_uint4(f16x2(o.x), f16x2(o.y), f16x2(o.z), f16x2(o.w));
               }
             }
             *reinterpret_cast<uint4*>(bt_base + sub * 2048 + swz(n, c)) = o;
@@ -341,16 +369,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = false;
             break;
           }
-          const uint32_t b_base = smem_addr(bring + bslot * BTB);
+          BFrags<WT, NT> bf;
+          bf.load(smem_addr(bring + bslot * BTB), lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&bempty[bslot]));
+          if (++bslot == kBStages) { bslot = 0; bp ^= 1u; }
 #pragma unroll
           for (int j = 0; j < kTileGroup; ++j) {
             if (j < ntile && ok) {
               if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&afull[aslot]), ap))) {
                 ok = false;
               } else {
-                const uint32_t a_base = smem_addr(aring + aslot * kATileBytes);
-                if constexpr (WT == MTP_W_BF16) stage_mma_bf16<NT>(a_base, b_base, acc[j], warp, lane);
-                else stage_mma_fp8<NT>(a_base, b_base, acc[j], warp, lane);
+                bf.mma(smem_addr(aring + aslot * kATileBytes), acc[j], warp, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&aempty[aslot]));
@@ -358,9 +388,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               }
             }
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&bempty[bslot]));
-          if (++bslot == kBStages) { bslot = 0; bp ^= 1u; }
         }
         if (!ok) break;
         // epilogue of the group: logits and per-sequence running argmax
