@@ -77,6 +77,7 @@ int run_input(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hn
   a.H = H;
   a.V = V;
   a.eps = eps;
+  a.inv_h = 1.0 / static_cast<double>(H);
   return map_cuda(mtp::launch_input_stage(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -97,6 +98,7 @@ int run_output(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_h
   a.H = H;
   a.V = V;
   a.eps = eps;
+  a.inv_h = 1.0 / static_cast<double>(H);
   return map_cuda(mtp::launch_sweep(a, static_cast<cudaStream_t>(stream)));
 }
 

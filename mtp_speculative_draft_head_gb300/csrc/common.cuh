@@ -444,16 +444,19 @@ __device__ void rms_norm_multi_to_smem(int njobs, int n, float eps, float* red, 
 
 // Sums of squares of nvec BF16 rows of n elements (n % 8 == 0, rows 16-byte aligned) as
 // double-floats (exact squares, TwoSum), for the batched kernels' norm prologues. Threads
-// 0..NT-1 call it (they synchronise on named barrier `bar`): NT / nvec consecutive threads share
-// a row, each loads kBatch 16-byte vectors at a time (independent loads in flight), and the
-// partials are added in thread order -- the result does not depend on timing. row(j) gives row
-// j (nullptr: a zero row). With kMax it also returns max_k |x_k * w_k| (exact products) for the
-// weight vector w. part / mpart: NT scratch entries; out / mout: nvec results.
+// 0..NT-1 call it (NT a multiple of 32; they synchronise on named barrier `bar`). A row is shared
+// by tpv threads, tpv the largest power of two with tpv * nvec <= NT; each thread loads kBatch
+// 16-byte vectors at a time (independent loads in flight), the tpv partials are combined by a
+// fixed shuffle butterfly (within a warp) and, when tpv > 32, the warp totals in warp order --
+// the result does not depend on timing. row(j) gives row j (nullptr: a zero row). With kMax it
+// also returns max_k |x_k * w_k| (exact products) for the weight vector w. part / mpart: NT / 32
+// scratch entries; out / mout: nvec results.
 template <int NT, int kBatch, bool kMax, class RowFn>
 __device__ void sumsq_rows(int nvec, int n, RowFn row, const uint16_t* w, DF* part, float* mpart, DF* out,
                            float* mout, int bar) {
-  const int tid = threadIdx.x;
-  const int tpv = NT / nvec;
+  const int tid = threadIdx.x, lane = tid & 31;
+  int tpv = 1;
+  while (tpv * 2 * nvec <= NT) tpv *= 2;
   const int j = tid / tpv, r = tid - j * tpv;
   const int nv = n >> 3;
   DF acc{0.0f, 0.0f};
@@ -491,18 +494,35 @@ __device__ void sumsq_rows(int nvec, int n, RowFn row, const uint16_t* w, DF* pa
       }
     }
   }
-  part[tid] = acc;
-  if constexpr (kMax) mpart[tid] = mx;
-  asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(NT) : "memory");
-  if (tid < nvec) {
-    DF tot = part[tid * tpv];
-    float m = kMax ? mpart[tid * tpv] : 0.0f;
-    for (int i = 1; i < tpv; ++i) {
-      tot = df_add(tot, part[tid * tpv + i]);
-      if constexpr (kMax) m = fmaxf(m, mpart[tid * tpv + i]);
+  // butterfly over the row's threads inside the warp (all lanes take part; groups are aligned)
+  const int span = tpv < 32 ? tpv : 32;
+  for (int m = span >> 1; m > 0; m >>= 1) {
+    acc = df_add(acc, shfl_xor_df(acc, m));
+    if constexpr (kMax) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+  }
+  if (tpv <= 32) {
+    if (r == 0 && j < nvec) {
+      out[j] = acc;
+      if constexpr (kMax) mout[j] = mx;
     }
-    out[tid] = tot;
-    if constexpr (kMax) mout[tid] = m;
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(NT) : "memory");
+  } else {
+    if (lane == 0) {
+      part[tid >> 5] = acc;
+      if constexpr (kMax) mpart[tid >> 5] = mx;
+    }
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(NT) : "memory");
+    const int wpv = tpv >> 5;  // warps per row
+    if (tid < nvec) {
+      DF tot = part[tid * wpv];
+      float m = kMax ? mpart[tid * wpv] : 0.0f;
+      for (int i = 1; i < wpv; ++i) {
+        tot = df_add(tot, part[tid * wpv + i]);
+        if constexpr (kMax) m = fmaxf(m, mpart[tid * wpv + i]);
+      }
+      out[tid] = tot;
+      if constexpr (kMax) mout[tid] = m;
+    }
   }
   asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(NT) : "memory");
 }

@@ -72,7 +72,8 @@ constexpr int kAStages = MTP_IN_ASTAGES;
 constexpr int kCells = kCK / 8;               // 16-byte cells per sequence row of a chunk
 constexpr int kBStep = kBW * 32 / kCells;     // sequences interleaved over the builder threads
 static_assert(kBW * 32 % kCells == 0 && kBStep >= 1, "builder threads must tile a chunk row");
-constexpr int kBarTokens = 3;                 // named barrier: tokens checked (prologue -> act producer)
+constexpr int kBarInRead = 3;                 // named barrier: prologue has read its inputs
+                                              // (prologue -> both producers)
 constexpr int kMaxTiles = 8;                  // n-tiles per CTA: at most 64 rows
 constexpr int kStepsPerWarp = kCK / 16 / kCW; // k16-steps of a chunk per consumer warp
 constexpr int kEpilogueBytes = kCW * kMaxTiles * 32 * 4 * 8;
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(kInTcThreads, 1)
     // Per k-chunk: the chunk's part of every sequence's embedding row (in range tokens only)
     // and target_hidden, and of enorm_w / hnorm_w, copied into the stage the builders then turn
     // into the concat in place.
-    asm volatile("bar.sync %0, %1;" ::"r"(kBarTokens), "r"(kPrologueThreads + 32) : "memory");
+    asm volatile("bar.sync %0, %1;" ::"r"(kBarInRead), "r"(kPrologueThreads + 64) : "memory");
     if (lane == 0) {
       const uint64_t policy = l2_evict_first_policy();
       int slot = 0, issued = 0;
@@ -180,6 +181,9 @@ __global__ void __launch_bounds__(kInTcThreads, 1)
     __syncwarp();
   } else if (warp == kProdWarp) {
     // ------------------------------------------------------------------ weight producer
+    // Both streams start once the prologue has read the embedding rows and target_hidden:
+    // issued first, ~20 MB of loads over all SMs sit in front of those in the memory queues.
+    asm volatile("bar.sync %0, %1;" ::"r"(kBarInRead), "r"(kPrologueThreads + 64) : "memory");
     if (lane == 0) {
       const uint64_t policy = l2_evict_first_policy();
       int slot = 0, issued = 0;
@@ -221,7 +225,6 @@ __global__ void __launch_bounds__(kInTcThreads, 1)
       if (!ok) store_status(a.status, MTP_ERR_TOKEN_RANGE);
     }
     named_barrier_sync(1, kPrologueThreads);
-    asm volatile("bar.arrive %0, %1;" ::"r"(kBarTokens), "r"(kPrologueThreads + 32) : "memory");
     {
       auto row = [&](int j) -> const uint16_t* {
         const int b = j >> 1;
@@ -229,11 +232,13 @@ __global__ void __launch_bounds__(kInTcThreads, 1)
         return valid_s[b] ? a.embed + static_cast<int64_t>(tok_s[b]) * H : nullptr;
       };
       sumsq_rows<kPrologueThreads, 8, false>(2 * B, H, row, nullptr, part, nullptr, tot, nullptr, 1);
+      asm volatile("bar.arrive %0, %1;" ::"r"(kBarInRead), "r"(kPrologueThreads + 64) : "memory");
       if (threadIdx.x < 2 * B) {
         const int b = threadIdx.x >> 1, half = threadIdx.x & 1;
         const DF t = tot[threadIdx.x];
-        const double ms = (static_cast<double>(t.hi) + static_cast<double>(t.lo)) / static_cast<double>(H);
-        const double rr = 1.0 / sqrt(ms + static_cast<double>(a.eps));
+        // 1 / rms in fp64 (rsqrt: within an ulp or two of the correctly rounded value)
+        const double ms = (static_cast<double>(t.hi) + static_cast<double>(t.lo)) * a.inv_h;
+        const double rr = rsqrt(ms + static_cast<double>(a.eps));
         const float rh = static_cast<float>(rr);
         nrm[(half * kMaxB + b) * 2] = rh;
         nrm[(half * kMaxB + b) * 2 + 1] = static_cast<float>(rr - static_cast<double>(rh));

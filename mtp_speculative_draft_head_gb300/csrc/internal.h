@@ -69,6 +69,7 @@ struct InputArgs {
   int32_t* status;
   int B, H, V;
   float eps;
+  double inv_h;  // 1 / H (fp64), for the mean of squares
   int stages;  // pipeline stages (bulk-copy kernel)
   int group;   // sequences whose concat is resident at once (plain kernel)
 };
@@ -85,6 +86,7 @@ struct SweepArgs {
   int w_dtype;
   int B, H, V;
   float eps;
+  double inv_h;  // 1 / H (fp64), for the mean of squares
   int stages;
 };
 

@@ -34,27 +34,35 @@ namespace mtp {
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kBuilderWarps = 4;
+constexpr int kBuilderWarps = 3;
 constexpr int kTcWarps = kConsumerWarps + kBuilderWarps + 1;
-constexpr int kTcThreads = kTcWarps * 32;          // 416
-constexpr int kPrologueThreads = (kConsumerWarps + kBuilderWarps) * 32;  // 384
+constexpr int kTcThreads = kTcWarps * 32;          // 384: three warps per SM sub-partition, so
+                                                   // up to 168 registers a thread
+constexpr int kPrologueThreads = (kConsumerWarps + kBuilderWarps) * 32;  // 352
 constexpr int kTileRows = 16 * kConsumerWarps;     // 128
-// Row tiles per group (their accumulators stay in registers while the activations of a k-block
-// are reused across them). 13 warps put 4 on one SM sub-partition, so a thread has at most 128
-// registers: the FP8 head with 16 sequences (two n-tiles, 32 registers of activation fragments)
-// takes groups of 4.
+// Row tiles per group (their accumulators stay in registers while the activations of a stage
+// are reused across them). With two n-tiles (B > 8) the FP8 activation fragments of a stage
+// take 64 registers, and its groups are 4 tiles.
 template <int WT, int NT>
-__host__ __device__ constexpr int tile_group() { return (WT == MTP_W_FP8_E4M3 && NT == 2) ? 4 : 8; }
-constexpr int kATileBytes = kTileRows * 128;       // 16 KB: 128 rows x 128 bytes
-constexpr int kAStages = 12;
-constexpr int kBStages = 4;
+__host__ __device__ constexpr int tile_group() { return (NT == 2 && WT == MTP_W_FP8_E4M3) ? 4 : 8; }
+constexpr int kATileBytes = kTileRows * 128;       // 16 KB: 128 rows x 128 bytes (one k-block)
+// A weight stage holds kKS consecutive k-blocks of one row tile (two tensor loads issued back to
+// back): each row is then read 256 contiguous bytes at a time. With one k-block per visit (128
+// bytes per row, the next 128 bytes only after the group's other 1023 rows) the same stream
+// reached 78% of the HBM bandwidth instead of 95%.
+constexpr int kKS = 2;
+constexpr int kAStageBytes = kKS * kATileBytes;    // 32 KB
+constexpr int kAStages = 6;
 constexpr int kSeq = 16;                           // activation rows per B tile (N <= 16)
 constexpr int kProducerWarp = kConsumerWarps + kBuilderWarps;
+constexpr int kBarXRead = 3;  // named barrier: prologue has read x (prologue -> producer)
 
 template <int WT>
 struct TcCfg {
   static constexpr int kKbElems = (WT == MTP_W_BF16) ? 64 : 128;  // weights per row per k-block
   static constexpr int kBTileBytes = kSeq * kKbElems * 2;         // bf16 / f16 activations
+  static constexpr int kBStageBytes = kKS * kBTileBytes;
+  static constexpr int kBStages = (WT == MTP_W_BF16) ? 4 : 3;
 };
 
 // ---------------------------------------------------------------------------- MMA of one stage
@@ -170,14 +178,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   using Cfg = TcCfg<WT>;
   constexpr int kTileGroup = tile_group<WT, NT>();
   constexpr int KBE = Cfg::kKbElems;
-  constexpr int BTB = Cfg::kBTileBytes;
+  constexpr int BTB = Cfg::kBTileBytes;     // activations of one k-block
+  constexpr int BSB = Cfg::kBStageBytes;    // one activation stage (kKS k-blocks)
+  constexpr int kBStages = Cfg::kBStages;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle pattern
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* aring = smem;
-  uint8_t* bring = aring + kAStages * kATileBytes;
-  uint64_t* afull = reinterpret_cast<uint64_t*>(bring + kBStages * BTB);
+  uint8_t* bring = aring + kAStages * kAStageBytes;
+  uint64_t* afull = reinterpret_cast<uint64_t*>(bring + kBStages * BSB);
   uint64_t* aempty = afull + kAStages;
   uint64_t* bfull = aempty + kAStages;
   uint64_t* bempty = bfull + kBStages;
@@ -189,6 +199,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int B = a.B, H = a.H;
   const int64_t V = a.V;
   const int KB = (H + KBE - 1) / KBE;
+  const int KP = (KB + kKS - 1) / kKS;  // weight / activation stages per row tile
   const int T = static_cast<int>((V + kTileRows - 1) / kTileRows);
   const int t0 = static_cast<int>(static_cast<int64_t>(T) * blockIdx.x / gridDim.x);
   const int t1 = static_cast<int>(static_cast<int64_t>(T) * (blockIdx.x + 1) / gridDim.x);
@@ -210,6 +221,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer
+    // The weight stream starts once the prologue has read x: issued first, ~30 MB of tensor
+    // loads over all SMs sit in front of those few loads in the memory queues and the prologue
+    // (hence the first MMA) comes several microseconds later.
+    asm volatile("bar.sync %0, %1;" ::"r"(kBarXRead), "r"(kPrologueThreads + 32) : "memory");
     int issued = 0;
     if (lane == 0) {
       const uint64_t policy = l2_evict_first_policy();
@@ -218,16 +233,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int gt = t0; gt < t1 && ok; gt += kTileGroup) {
         const int ntile = (t1 - gt) < kTileGroup ? (t1 - gt) : kTileGroup;
-        for (int kb = 0; kb < KB && ok; ++kb) {
+        for (int kp = 0; kp < KP && ok; ++kp) {
+          const int nsub = KB - kp * kKS < kKS ? KB - kp * kKS : kKS;
           for (int j = 0; j < ntile; ++j) {
             if (*reinterpret_cast<volatile int*>(&abort_flag) || !mbar_wait_bounded(smem_addr(&aempty[slot]), ep)) {
               ok = false;
               break;
             }
             const uint32_t bar = smem_addr(&afull[slot]);
-            mbar_arrive_expect_tx(bar, kATileBytes);
-            tma_load_2d(smem_addr(aring + slot * kATileBytes), &tmap_w, kb * KBE, (gt + j) * kTileRows, bar,
-                        policy);
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nsub * kATileBytes));
+            for (int sb = 0; sb < nsub; ++sb)
+              tma_load_2d(smem_addr(aring + slot * kAStageBytes + sb * kATileBytes), &tmap_w, (kp * kKS + sb) * KBE,
+                          (gt + j) * kTileRows, bar, policy);
             ++issued;
             if (++slot == kAStages) { slot = 0; ep ^= 1u; }
           }
@@ -255,10 +272,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float* mtot = reinterpret_cast<float*>(tot + kSeq);
       auto row = [&](int b) -> const uint16_t* { return a.x + static_cast<size_t>(b) * H; };
       sumsq_rows<kPrologueThreads, 8, WT == MTP_W_FP8_E4M3>(B, H, row, a.final_norm_w, part, mpart, tot, mtot, 1);
+      asm volatile("bar.arrive %0, %1;" ::"r"(kBarXRead), "r"(kPrologueThreads + 32) : "memory");
       if (threadIdx.x < B) {
         const int b = threadIdx.x;
-        const double ms = (static_cast<double>(tot[b].hi) + static_cast<double>(tot[b].lo)) / static_cast<double>(H);
-        const double rr = 1.0 / sqrt(ms + static_cast<double>(a.eps));
+        // 1 / rms in fp64 (rsqrt: within an ulp or two of the correctly rounded value)
+        const double ms = (static_cast<double>(tot[b].hi) + static_cast<double>(tot[b].lo)) * a.inv_h;
+        const double rr = rsqrt(ms + static_cast<double>(a.eps));
         const float rh = static_cast<float>(rr);
         const float rl = static_cast<float>(rr - static_cast<double>(rh));
         nrm[b] = rh;
@@ -286,55 +305,77 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp >= kConsumerWarps) {
       // ---------------------------------------------------------------- builders
-      const int bt = threadIdx.x - kConsumerWarps * 32;  // 0..127
-      const int n = bt >> 3, c = bt & 7;
-      const bool live = n < B;
-      const float rh = live ? nrm[n] : 0.0f, rl = live ? nrm[kSeq + n] : 0.0f;
-      const float xs = live ? nrm[2 * kSeq + n] : 1.0f;
-      const uint16_t* xrow = a.x + static_cast<size_t>(live ? n : 0) * H;
+      // A sub-tile has 16 sequences x 8 cells of 16 bytes; this thread's cells are bt, bt + 96.
+      // The stages follow one another over the groups (u = group * KP + kp); the x / weight
+      // vectors of stage u + 1 are loaded into registers as soon as stage u is published, so
+      // their latency overlaps the wait for the next free slot.
+      constexpr int kSubs = BSB / 2048;
+      constexpr int kCellIt = (kSeq * 8 + kBuilderWarps * 32 - 1) / (kBuilderWarps * 32);
+      const int bt = threadIdx.x - kConsumerWarps * 32;  // 0..95
+      const int ngroups = (t1 - t0 + kTileGroup - 1) / kTileGroup;
+      const int nstages = ngroups * KP;
+      uint4 xr[kSubs][kCellIt], wr[kSubs][kCellIt];
+      auto fetch = [&](int u) {
+        const int kp = u % KP;
+#pragma unroll
+        for (int sub = 0; sub < kSubs; ++sub)
+#pragma unroll
+          for (int ci = 0; ci < kCellIt; ++ci) {
+            const int cell = bt + ci * kBuilderWarps * 32;
+            const int n = cell >> 3, c = cell & 7;
+            const int k0 = kp * kKS * KBE + 64 * sub + 8 * c;
+            if (cell < kSeq * 8 && n < B && k0 < H) {
+              xr[sub][ci] = *reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(n) * H + k0);
+              wr[sub][ci] = *reinterpret_cast<const uint4*>(a.final_norm_w + k0);
+            }
+          }
+      };
+      if (nstages > 0) fetch(0);
       int slot = 0;
       uint32_t ep = 1;
-      for (int gt = t0; gt < t1; gt += kTileGroup) {
-        bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (*reinterpret_cast<volatile int*>(&abort_flag) ||
-              !__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&bempty[slot]), ep))) {
-            ok = false;
-            break;
-          }
-          uint8_t* bt_base = bring + slot * BTB;
-#pragma unroll
-          for (int sub = 0; sub < BTB / 2048; ++sub) {
-            const int k0 = kb * KBE + 64 * sub + 8 * c;
-            uint4 o = make_uint4(0u, 0u, 0u, 0u);
-            if (live && k0 < H) {
-              const uint4 xq = *reinterpret_cast<const uint4*>(xrow + k0);
-              const uint4 wq = *reinterpret_cast<const uint4*>(a.final_norm_w + k0);
-              const uint32_t xu[4] = {xq.x, xq.y, xq.z, xq.w};
-              const float wf[8] = {bf16_lo(wq.x), bf16_hi(wq.x), bf16_lo(wq.y), bf16_hi(wq.y),
-                                   bf16_lo(wq.z), bf16_hi(wq.z), bf16_lo(wq.w), bf16_hi(wq.w)};
-              o = bf16x8_scaled_rne(xu, wf, rh, rl);  // xhat, BF16
-              if constexpr (WT == MTP_W_FP8_E4M3) {
-                // f16 of xhat * 2^k (exact inside the f16 range)
-                auto f16x2 = [xs](uint32_t v) {
-                  return f16_bits(__fmul_rn(bf16_lo(v), xs)) | (f16_bits(__fmul_rn(bf16_hi(v), xs)) << 16);
-                };
-                o = make_uint4(f16x2(o.x), f16x2(o.y), f16x2(o.z), f16x2(o.w));
-              }
-            }
-            *reinterpret_cast<uint4*>(bt_base + sub * 2048 + swz(n, c)) = o;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&bfull[slot]));
-          if (++slot == kBStages) { slot = 0; ep ^= 1u; }
-        }
-        if (!ok) {
+      for (int u = 0; u < nstages; ++u) {
+        const int kp = u % KP;
+        if (*reinterpret_cast<volatile int*>(&abort_flag) ||
+            !__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&bempty[slot]), ep))) {
           if (lane == 0) {
             store_status(a.status, MTP_ERR_TIMEOUT);
             atomicExch(&abort_flag, 1);
           }
           break;
         }
+        uint8_t* bt_base = bring + slot * BSB;
+        // 2 KB sub-tiles of 64 activations x 16 sequences, k-block-major (zeros past H)
+#pragma unroll
+        for (int sub = 0; sub < kSubs; ++sub)
+#pragma unroll
+          for (int ci = 0; ci < kCellIt; ++ci) {
+            const int cell = bt + ci * kBuilderWarps * 32;
+            const int n = cell >> 3, c = cell & 7;
+            const int k0 = kp * kKS * KBE + 64 * sub + 8 * c;
+            if (cell < kSeq * 8) {
+              uint4 o = make_uint4(0u, 0u, 0u, 0u);
+              if (n < B && k0 < H) {
+                const uint4 xq = xr[sub][ci], wq = wr[sub][ci];
+                const uint32_t xu[4] = {xq.x, xq.y, xq.z, xq.w};
+                const float wf[8] = {bf16_lo(wq.x), bf16_hi(wq.x), bf16_lo(wq.y), bf16_hi(wq.y),
+                                     bf16_lo(wq.z), bf16_hi(wq.z), bf16_lo(wq.w), bf16_hi(wq.w)};
+                o = bf16x8_scaled_rne(xu, wf, nrm[n], nrm[kSeq + n]);  // xhat, BF16
+                if constexpr (WT == MTP_W_FP8_E4M3) {
+                  // f16 of xhat * 2^k (exact inside the f16 range)
+                  const float xs = nrm[2 * kSeq + n];
+                  auto f16x2 = [xs](uint32_t v) {
+                    return f16_bits(__fmul_rn(bf16_lo(v), xs)) | (f16_bits(__fmul_rn(bf16_hi(v), xs)) << 16);
+                  };
+                  o = make_uint4(f16x2(o.x), f16x2(o.y), f16x2(o.z), f16x2(o.w));
+                }
+              }
+              *reinterpret_cast<uint4*>(bt_base + sub * 2048 + swz(n, c)) = o;
+            }
+          }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&bfull[slot]));
+        if (++slot == kBStages) { slot = 0; ep ^= 1u; }
+        if (u + 1 < nstages) fetch(u + 1);
       }
     } else {
       // ---------------------------------------------------------------- consumers
@@ -363,14 +404,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (j < ntile && r0 + 8 < V) scl[j][1] = __ldg(a.scale + r0 + 8);
           }
         }
-        for (int kb = 0; kb < KB && ok; ++kb) {
+        for (int kp = 0; kp < KP && ok; ++kp) {
+          const int nsub = KB - kp * kKS < kKS ? KB - kp * kKS : kKS;
           if (*reinterpret_cast<volatile int*>(&abort_flag) ||
               !__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&bfull[bslot]), bp))) {
             ok = false;
             break;
           }
-          BFrags<WT, NT> bf;
-          bf.load(smem_addr(bring + bslot * BTB), lane);
+          BFrags<WT, NT> bf[kKS];
+#pragma unroll
+          for (int sb = 0; sb < kKS; ++sb) bf[sb].load(smem_addr(bring + bslot * BSB + sb * BTB), lane);
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&bempty[bslot]));
           if (++bslot == kBStages) { bslot = 0; bp ^= 1u; }
@@ -380,7 +423,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&afull[aslot]), ap))) {
                 ok = false;
               } else {
-                bf.mma(smem_addr(aring + aslot * kATileBytes), acc[j], warp, lane);
+#pragma unroll
+                for (int sb = 0; sb < kKS; ++sb)
+                  if (sb < nsub) bf[sb].mma(smem_addr(aring + aslot * kAStageBytes + sb * kATileBytes), acc[j], warp, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&aempty[aslot]));
@@ -451,9 +496,10 @@ cudaError_t launch_tc(const SweepArgs& a, const CUtensorMap& tm, unsigned grid, 
 }  // namespace
 
 size_t sweep_tc_smem_bytes(int w_dtype) {
-  const int btb = (w_dtype == MTP_W_BF16) ? TcCfg<MTP_W_BF16>::kBTileBytes : TcCfg<MTP_W_FP8_E4M3>::kBTileBytes;
-  return 1024 + static_cast<size_t>(kAStages) * kATileBytes + static_cast<size_t>(kBStages) * btb +
-         (2 * kAStages + 2 * kBStages) * 8 + 4 * kSeq * 4 + kTcWarps * kSeq * sizeof(ArgBest) + 64;
+  const int bsb = (w_dtype == MTP_W_BF16) ? TcCfg<MTP_W_BF16>::kBStageBytes : TcCfg<MTP_W_FP8_E4M3>::kBStageBytes;
+  const int nbs = (w_dtype == MTP_W_BF16) ? TcCfg<MTP_W_BF16>::kBStages : TcCfg<MTP_W_FP8_E4M3>::kBStages;
+  return 1024 + static_cast<size_t>(kAStages) * kAStageBytes + static_cast<size_t>(nbs) * bsb +
+         (2 * kAStages + 2 * nbs) * 8 + 4 * kSeq * 4 + kTcWarps * kSeq * sizeof(ArgBest) + 64;
 }
 
 cudaError_t launch_sweep_tc(const SweepArgs& a, cudaStream_t stream, bool* launched) {
