@@ -9,7 +9,8 @@ lm_head sweep, argmax) -- 2.05 GB of weights streamed per step, 16x the L2, so e
 HBM. The timed steps are one CUDA-graph replay of the K-step chain.
 
 Reported: value = algorithmic HBM bytes per step / time per step (GB/s, all ranks), the sweep
-kernel's roofline (a timed loop of back-to-back sweeps), the same for the FP8 E4M3 head, an
+kernel's roofline (a timed loop of back-to-back sweeps), the same for the FP8 E4M3 head, batched
+drafting (B = 2, 4, 8, 16 sequences per step: full head and sweep alone, BF16 and FP8), an
 end-to-end figure through the host-buffer C entry point (host->device inputs and the draft back
 each step), SM clocks sampled during the timed loops, and the CPU oracle on a bounded sample.
 
@@ -39,6 +40,7 @@ import synth  # noqa: E402
 
 METRIC = "lm_head draft sweep µs and HBM GB/s (BF16/FP8, H=6144, V=154880, B=1)"
 H, V, B = 6144, 154880, 1
+BATCHES = (2, 4, 8, 16)
 EPS = synth.EPS
 CHAIN = 1000
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -267,6 +269,49 @@ def run_ours(args, world, rank, local):
     for g in graphs.values():  # one untimed replay each
         g.replay()
     torch.cuda.synchronize()
+    # batched drafting (B sequences per step, one pass over the weights): a shorter chain of
+    # Kb steps per B, BF16 and FP8, plus the sweep alone
+    Kb = max(1, min(K, 20))
+    bgraphs = {}
+    for b in BATCHES:
+        tokens_b, hidden_b = synth.make_step_inputs(H, V, b, 1000 + b, dev)
+        tokb = torch.empty((Kb + 1, b), dtype=torch.int32, device=dev)
+        tokb[0].copy_(tokens_b)
+        xb = torch.empty((b, H), dtype=torch.bfloat16, device=dev)
+        db = torch.empty(b, dtype=torch.int32, device=dev)
+
+        def chain_b(n, fp8, tokb=tokb, hidden_b=hidden_b, xb=xb):
+            Wt, s, wt = head._head(fp8)
+
+            def fn(st):
+                for i in range(n):
+                    m.mtp_head_forward_batched(head.embed, head.enorm_w, head.hnorm_w, head.eh_proj,
+                                               head.final_norm_w, Wt, s, wt, tokb[i], hidden_b, xb, None,
+                                               tokb[i + 1], head.ws, status, EPS, st)
+            return fn
+
+        def sweep_b(n, fp8, xb=xb, db=db):
+            Wt, s, wt = head._head(fp8)
+
+            def fn(st):
+                for _ in range(n):
+                    m.mtp_head_logits_argmax_batched(xb, head.final_norm_w, Wt, s, wt, None, db, head.ws, status,
+                                                     EPS, st)
+            return fn
+
+        with torch.cuda.stream(stream):
+            for fp8 in (False, True):
+                chain_b(max(W, 3), fp8)(stream)
+                sweep_b(max(W, 3), fp8)(stream)
+        torch.cuda.synchronize()
+        for fp8 in (False, True):
+            bgraphs[(b, "chain", fp8)] = capture(chain_b(Kb, fp8))
+            bgraphs[(b, "sweep", fp8)] = capture(sweep_b(Kb, fp8))
+    torch.cuda.synchronize()
+    for g in bgraphs.values():
+        g.replay()
+    torch.cuda.synchronize()
+
     launches_all = 0
     with ClockSampler(local) as clocks:
         for key in (("chain", False), ("chain", True), ("sweep", False), ("sweep", True), ("input", None)):
@@ -275,6 +320,11 @@ def run_ours(args, world, rank, local):
             barrier(world)
             results[key] = ms
             launches_all += 2 * K if key[0] == "chain" else K
+        for key, g in bgraphs.items():
+            barrier(world)
+            results[key] = timed_graph(g, torch.cuda.current_stream())
+            barrier(world)
+            launches_all += 2 * Kb if key[1] == "chain" else Kb
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}: {m.strerror(int(status.item()))}")
     drafts = tok[1:K + 1].view(-1)
@@ -315,6 +365,19 @@ def run_ours(args, world, rank, local):
     e2e_gbs = step_bytes(2) * ke * world / (e2e_ms * 1e-3) / 1e9
 
     peak, peak_src = peak_hbm()
+    batched = {}
+    for b in BATCHES:
+        e = {}
+        for fp8, tag, wb in ((False, "bf16", 2), (True, "fp8", 1)):
+            ch = aggregate(results[(b, "chain", fp8)], input_bytes(b) + sweep_bytes(wb, b), Kb, world)
+            sw = aggregate(results[(b, "sweep", fp8)], sweep_bytes(wb, b), Kb, world)
+            e[f"head_{tag}_us"] = round(ch["ms_per_step"] * 1e3, 2)
+            e[f"tokens_per_s_{tag}"] = round(b * world / (ch["ms_per_step"] * 1e-3), 1)
+            e[f"sweep_{tag}_us"] = round(sw["ms_per_step"] * 1e3, 2)
+            e[f"sweep_{tag}_gbs"] = round(sw["gbs"], 1)
+            e[f"sweep_{tag}_frac"] = round(sw["gbs"] / world / peak, 4)
+        e["input_us_approx"] = round(e["head_bf16_us"] - e["sweep_bf16_us"], 2)
+        batched[f"B={b}"] = e
     kname = "sweep_regx_kernel<BF16,H=6144,B=1>"
     achieved = sweep_bytes(2) / (results[("sweep", False)] / K * 1e-3) / 1e9
     line = {
@@ -350,6 +413,8 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "us_per_step": round(e2e_ms / ke * 1e3, 2),
                 "h2d_bytes_per_step": 4 + H * 2, "d2h_bytes_per_step": 4, "steps": ke,
                 "api": "mtp_head_forward_host (pinned host buffers, synchronous per step)"},
+        "batched": dict(batched, steps=Kb, kernels="tensor-core input stage and sweep (mma.sync)",
+                        timing="Kb-step chains / sweep loops in one CUDA graph each; frac of the measured peak"),
         "gpu_launches": 2 * K,  # the BF16 chain region `value` is timed on: 2 kernels per step
         "gpu_launches_all_timed_regions": launches_all,
         "clocks": clocks.summary(),
