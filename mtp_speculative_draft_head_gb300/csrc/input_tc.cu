@@ -17,13 +17,15 @@
 // N operand of the MMA, one group per n-tile; the batch is the M operand (16 sequences, rows
 // >= B ignored). No split over k between CTAs, so no workspace and no atomics.
 //  * weight producer warp: one 3-D tensor load per stage (8 rows x 1024 elements, 16 KB, L2
-//    evict-first, 128-byte swizzle so the ldmatrix reads are bank-conflict free) into an
-//    8-stage ring -- few large copies: the same stream in 1 KB row pieces ran at a third of
+//    evict-first, 128-byte swizzle so the ldmatrix reads are bank-conflict free) into a
+//    7-stage ring -- few large copies: the same stream in 1 KB row pieces ran at a third of
 //    the bandwidth;
 //  * activation producer warp: per 1024-element k-chunk, bulk copies of the chunk's part of
 //    every embedding row (gathered by token) or target_hidden row and of enorm_w / hnorm_w into
-//    a 2-stage ring, so the builders never wait on a global load;
-//  * 4 builder warps: turn a stage in place into the normalised concat of all B sequences
+//    a 3-stage ring, so the builders never wait on a global load (a stage is held from its copy
+//    through building to its last MMA, so the third stage matters more than an eighth weight
+//    stage);
+//  * 6 builder warps: turn a stage in place into the normalised concat of all B sequences
 //    (rms_norm_vanilla with enorm / hnorm, correctly rounded to BF16 exactly as the
 //    single-sequence kernel does);
 //  * 8 consumer warps: each owns 8 of the 64 k16-steps of a chunk for every n-tile of the CTA;
@@ -44,8 +46,11 @@ namespace mtp {
 
 namespace {
 
+#ifndef MTP_IN_BUILDERS
+#define MTP_IN_BUILDERS 6
+#endif
 constexpr int kCW = 8;                        // consumer warps
-constexpr int kBW = 4;                        // builder warps
+constexpr int kBW = MTP_IN_BUILDERS;          // builder warps
 constexpr int kProdWarp = kCW + kBW;          // weight producer warp
 constexpr int kActWarp = kProdWarp + 1;       // activation producer warp
 constexpr int kInTcThreads = (kCW + kBW + 2) * 32;
@@ -54,10 +59,10 @@ constexpr int kPrologueThreads = (kCW + kBW) * 32;
 #define MTP_IN_CK 1024
 #endif
 #ifndef MTP_IN_WSTAGES
-#define MTP_IN_WSTAGES (MTP_IN_CK == 512 ? 16 : 8)
+#define MTP_IN_WSTAGES (MTP_IN_CK == 512 ? 14 : 7)
 #endif
 #ifndef MTP_IN_ASTAGES
-#define MTP_IN_ASTAGES (MTP_IN_CK == 512 ? 4 : 2)
+#define MTP_IN_ASTAGES (MTP_IN_CK == 512 ? 6 : 3)
 #endif
 #ifndef MTP_IN_FENCE
 #define MTP_IN_FENCE 1
@@ -70,8 +75,6 @@ constexpr int kAWOffset = kMaxB * kPitch;     // norm-weight segment after the 1
 constexpr int kAStageBytes = kAWOffset + kCK * 2;
 constexpr int kAStages = MTP_IN_ASTAGES;
 constexpr int kCells = kCK / 8;               // 16-byte cells per sequence row of a chunk
-constexpr int kBStep = kBW * 32 / kCells;     // sequences interleaved over the builder threads
-static_assert(kBW * 32 % kCells == 0 && kBStep >= 1, "builder threads must tile a chunk row");
 constexpr int kBarInRead = 3;                 // named barrier: prologue has read its inputs
                                               // (prologue -> both producers)
 constexpr int kMaxTiles = 8;                  // n-tiles per CTA: at most 64 rows
@@ -252,9 +255,8 @@ __global__ void __launch_bounds__(kInTcThreads, 1)
       // The stage holds the raw BF16 inputs of this chunk (row b: embedding / target_hidden
       // segment; then the norm-weight segment); each 8-element piece is replaced in place by its
       // normalised, correctly rounded concat values.
-      // thread -> one 16-byte column c of the chunk, for sequences bsub, bsub + kBStep, ...
-      const int bt = threadIdx.x - kCW * 32;  // 0..127
-      const int c = bt % kCells, bsub = bt / kCells;
+      // thread -> 16-byte cells bt, bt + 32 * kBW, ... of the chunk (sequence-major)
+      const int bt = threadIdx.x - kCW * 32;
       int slot = 0;
       uint32_t xp = 0;
       for (int kc = 0; kc < nck; ++kc) {
@@ -269,21 +271,21 @@ __global__ void __launch_bounds__(kInTcThreads, 1)
           break;
         }
         uint8_t* base = aring + slot * kAStageBytes;
-        if (c < ppr) {
-          const int half = k0 + 8 * c >= H ? 1 : 0;
-          const uint4 wq = *reinterpret_cast<const uint4*>(base + kAWOffset + c * 16);
-          const float wf[8] = {bf16_lo(wq.x), bf16_hi(wq.x), bf16_lo(wq.y), bf16_hi(wq.y),
-                               bf16_lo(wq.z), bf16_hi(wq.z), bf16_lo(wq.w), bf16_hi(wq.w)};
-#pragma unroll 4
-          for (int b = bsub; b < B; b += kBStep) {
-            uint4* cell = reinterpret_cast<uint4*>(base + b * kPitch + c * 16);
+        for (int cell = bt; cell < B * kCells; cell += kBW * 32) {
+          const int b = cell / kCells, c = cell - b * kCells;
+          if (c < ppr) {
+            const int half = k0 + 8 * c >= H ? 1 : 0;
+            uint4* cp = reinterpret_cast<uint4*>(base + b * kPitch + c * 16);
             uint4 o = make_uint4(0u, 0u, 0u, 0u);
             if (half || valid_s[b]) {
-              const uint4 xq = *cell;
+              const uint4 wq = *reinterpret_cast<const uint4*>(base + kAWOffset + c * 16);
+              const float wf[8] = {bf16_lo(wq.x), bf16_hi(wq.x), bf16_lo(wq.y), bf16_hi(wq.y),
+                                   bf16_lo(wq.z), bf16_hi(wq.z), bf16_lo(wq.w), bf16_hi(wq.w)};
+              const uint4 xq = *cp;
               const uint32_t xu[4] = {xq.x, xq.y, xq.z, xq.w};
               o = bf16x8_scaled_rne(xu, wf, nrm[(half * kMaxB + b) * 2], nrm[(half * kMaxB + b) * 2 + 1]);
             }
-            *cell = o;
+            *cp = o;
           }
         }
         fence_proxy_async_smem();  // the stage is refilled by bulk copies once consumed
