@@ -290,6 +290,30 @@ __device__ __forceinline__ void arg_update(ArgBest& b, float v, int32_t i) {
   }
 }
 
+// Last step of the grid argmax: combine the per-CTA partials part[g * nb + b] (g < ncta) into
+// draft[b]. One warp per sequence; its lanes read partials g = lane, lane + 32, ... at once
+// (a single thread walking all partials waited out one L2 latency per CTA, ~30 us for 152)
+// and a shuffle tree combines them. (value, lowest index) is a total order, so the result does
+// not depend on the order. All threads of the block call it.
+__device__ __forceinline__ void combine_partials(const ArgBest* part, unsigned int ncta, int nb, int32_t* draft) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int b = warp; b < nb; b += nw) {
+    ArgBest c{0.0f, -1};
+    for (unsigned int g = lane; g < ncta; g += 32) {
+      const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(part + static_cast<size_t>(g) * nb + b));
+      const int32_t i = static_cast<int32_t>(raw.y);
+      if (i >= 0) arg_update(c, __uint_as_float(raw.x), i);
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+      const float v = __shfl_xor_sync(0xffffffffu, c.v, m);
+      const int32_t i = __shfl_xor_sync(0xffffffffu, c.i, m);
+      if (i >= 0) arg_update(c, v, i);
+    }
+    if (lane == 0) draft[b] = c.i;
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 // Packed fp32 pairs (sm_100+ f32x2 instructions): two IEEE round-to-nearest operations per
 // instruction, lane-wise identical to the scalar ones.

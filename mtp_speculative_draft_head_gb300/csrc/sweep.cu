@@ -70,15 +70,7 @@ __device__ void argmax_finish(const ArgBest* best, int nb, ArgBest* wbest, uint8
   __syncthreads();
   if (is_last) {
     __threadfence();
-    if (threadIdx.x < nb) {
-      ArgBest c{0.0f, -1};
-      for (unsigned int g = 0; g < gridDim.x; ++g) {
-        const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(part + g * nb + threadIdx.x));
-        const ArgBest o{__uint_as_float(raw.x), static_cast<int32_t>(raw.y)};
-        if (o.i >= 0) arg_update(c, o.v, o.i);
-      }
-      draft[threadIdx.x] = c.i;
-    }
+    combine_partials(part, gridDim.x, nb, draft);
     if (threadIdx.x == 0) atomicExch(counter, 0u);
   }
 }

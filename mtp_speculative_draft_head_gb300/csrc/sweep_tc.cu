@@ -158,15 +158,7 @@ __device__ void tc_argmax_finish(int nb, const ArgBest* wbest, uint8_t* ws, int3
   __syncthreads();
   if (is_last) {
     __threadfence();
-    if (threadIdx.x < nb) {
-      ArgBest c{0.0f, -1};
-      for (unsigned int gi = 0; gi < gridDim.x; ++gi) {
-        const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(part + gi * nb + threadIdx.x));
-        const ArgBest o{__uint_as_float(raw.x), static_cast<int32_t>(raw.y)};
-        if (o.i >= 0) arg_update(c, o.v, o.i);
-      }
-      draft[threadIdx.x] = c.i;
-    }
+    combine_partials(part, gridDim.x, nb, draft);
     if (threadIdx.x == 0) atomicExch(counter, 0u);
   }
 }
