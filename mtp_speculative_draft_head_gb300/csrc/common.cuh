@@ -374,7 +374,8 @@ __device__ __forceinline__ DF df2_y(const DF2& a) { return DF{f2_hi(a.hi), f2_hi
 // The sums of squares are double-floats (each square of a BF16 value is exact in fp32), 1/rms is
 // formed in fp64 and split into two fp32 parts, and x*w (exact in fp32) times 1/rms is rounded
 // once to BF16 from a double-float -- so each output is the correctly rounded BF16 of the fp64
-// expression unless that lies within ~2^-40 relative of a rounding midpoint.
+// expression unless that lies within ~2^-40 relative of a rounding midpoint (1/rms is fp64 rsqrt,
+// within an ulp or two of the correctly rounded fp64 value).
 // One pass over the inputs, one block reduction for all vectors. All NT threads of the block
 // call it; `red` holds >= njobs * (2 * NT / 32 + 2) floats. A job with valid == false writes
 // zeros without reading x.
@@ -386,49 +387,190 @@ struct NormJob {
   bool valid;
 };
 
-template <int NT, class Layout, class JobFn>
-__device__ void rms_norm_multi_to_smem(int njobs, int n, float eps, float* red, JobFn job,
-                                       Layout layout) {
+struct NoOp {
+  __device__ __forceinline__ void operator()() const {}
+};
+
+template <int NT, class Layout, class JobFn, class AfterLoads = NoOp>
+__device__ void rms_norm_multi_to_smem(int njobs, int n, double inv_n, float eps, float* red, JobFn job,
+                                       Layout layout, AfterLoads after_loads = AfterLoads{}) {
   constexpr int NW = NT / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int j = 0; j < njobs; ++j) {
-    const NormJob J = job(j);
-    DF acc{0.0f, 0.0f};
-    if (J.valid) {
-      const bool vec = ((n & 7) == 0) && ((reinterpret_cast<uintptr_t>(J.x) & 15u) == 0);
-      if (vec) {
-        const uint4* xv = reinterpret_cast<const uint4*>(J.x);
-        for (int v = tid; v < n / 8; v += NT) {
-          const uint4 q = xv[v];
-          const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+  {
+    // One or two vectors of up to 2 * NT 16-byte pieces (the single-sequence kernels): each
+    // thread keeps its x and w pieces in registers from the first pass to the second. By the
+    // second pass the shared memory is mostly stage buffers, L1 no longer holds x, and
+    // re-reading it behind the weight stream took several us.
+    constexpr int KC = 2;
+    const NormJob J0 = job(0);
+    const NormJob J1 = njobs > 1 ? job(1) : NormJob{nullptr, nullptr, nullptr, false};
+    auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const bool fits = njobs <= 2 && (n & 7) == 0 && n / 8 <= KC * NT && (!J0.valid || (al(J0.x) && al(J0.w))) &&
+                      (!J1.valid || (al(J1.x) && al(J1.w)));
+    if (fits) {
+      const int nv = n / 8;
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      uint4 xq[2][KC], wq[2][KC];
+#pragma unroll
+      for (int i = 0; i < KC; ++i) {
+        const int v = tid + i * NT;
+        xq[0][i] = (J0.valid && v < nv) ? reinterpret_cast<const uint4*>(J0.x)[v] : z;
+        xq[1][i] = (J1.valid && v < nv) ? reinterpret_cast<const uint4*>(J1.x)[v] : z;
+        wq[0][i] = (J0.valid && v < nv) ? reinterpret_cast<const uint4*>(J0.w)[v] : z;
+        wq[1][i] = (J1.valid && v < nv) ? reinterpret_cast<const uint4*>(J1.w)[v] : z;
+      }
+      DF acc[2] = {DF{0.0f, 0.0f}, DF{0.0f, 0.0f}};
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int i = 0; i < KC; ++i) {
+          const uint32_t u[4] = {xq[jj][i].x, xq[jj][i].y, xq[jj][i].z, xq[jj][i].w};
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             const float a = bf16_lo(u[t]), b = bf16_hi(u[t]);
-            df_add(acc, __fmul_rn(a, a));
-            df_add(acc, __fmul_rn(b, b));
+            df_add(acc[jj], __fmul_rn(a, a));
+            df_add(acc[jj], __fmul_rn(b, b));
           }
         }
-      } else {
-        for (int k = tid; k < n; k += NT) {
-          const float a = bf16_bits_to_f32(J.x[k]);
+      after_loads();
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) {
+        acc[0] = df_add(acc[0], shfl_xor_df(acc[0], m));
+        acc[1] = df_add(acc[1], shfl_xor_df(acc[1], m));
+      }
+      if (lane == 0)
+        for (int jj = 0; jj < njobs; ++jj) {
+          red[(jj * NW + warp) * 2] = acc[jj].hi;
+          red[(jj * NW + warp) * 2 + 1] = acc[jj].lo;
+        }
+      __syncthreads();
+      float* rr = red + njobs * NW * 2;
+      if (tid < njobs) {
+        DF tot{red[tid * NW * 2], red[tid * NW * 2 + 1]};
+        for (int i = 1; i < NW; ++i) tot = df_add(tot, DF{red[(tid * NW + i) * 2], red[(tid * NW + i) * 2 + 1]});
+        // 1 / rms in fp64 (rsqrt: within an ulp or two of the correctly rounded value)
+        const double ms = (static_cast<double>(tot.hi) + static_cast<double>(tot.lo)) * inv_n;
+        const double r = rsqrt(ms + static_cast<double>(eps));
+        const float rh = static_cast<float>(r);
+        rr[2 * tid] = rh;
+        rr[2 * tid + 1] = static_cast<float>(r - static_cast<double>(rh));
+      }
+      __syncthreads();
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        if (jj < njobs) {
+          const NormJob J = jj == 0 ? J0 : J1;
+          const float rh = rr[2 * jj], rl = rr[2 * jj + 1];
+#pragma unroll
+          for (int i = 0; i < KC; ++i) {
+            const int v = tid + i * NT;
+            if (v < nv) {
+              uint4 o = z;
+              if (J.valid) {
+                const uint32_t xu[4] = {xq[jj][i].x, xq[jj][i].y, xq[jj][i].z, xq[jj][i].w};
+                const uint4 w4 = wq[jj][i];
+                const float wf[8] = {bf16_lo(w4.x), bf16_hi(w4.x), bf16_lo(w4.y), bf16_hi(w4.y),
+                                     bf16_lo(w4.z), bf16_hi(w4.z), bf16_lo(w4.w), bf16_hi(w4.w)};
+                o = bf16x8_scaled_rne(xu, wf, rh, rl);
+              }
+              // 8 consecutive elements starting at a multiple of 8 stay consecutive in every layout
+              *reinterpret_cast<uint4*>(J.out + layout(8 * v)) = o;
+            }
+          }
+        }
+      }
+      return;
+    }
+  }
+  // Sums of squares, two vectors at a time with their loads in flight together (one memory
+  // round trip per pair, not per vector), software-pipelined by one step; the weight vectors
+  // are prefetched into L2 alongside (the second pass reads them). after_loads() runs once the
+  // first pair has been read: the caller can start its own heavy traffic then, without
+  // putting it in front of these reads.
+  bool called = false;
+  for (int j0 = 0; j0 < njobs; j0 += 2) {
+    const NormJob J0 = job(j0);
+    const NormJob J1 = (j0 + 1 < njobs) ? job(j0 + 1) : NormJob{nullptr, nullptr, nullptr, false};
+    auto vec_ok = [n](const NormJob& J) {
+      return !J.valid || (((n & 7) == 0) && ((reinterpret_cast<uintptr_t>(J.x) & 15u) == 0));
+    };
+    DF acc0{0.0f, 0.0f}, acc1{0.0f, 0.0f};
+    if (vec_ok(J0) && vec_ok(J1)) {
+      const uint4* x0 = reinterpret_cast<const uint4*>(J0.x);
+      const uint4* x1 = reinterpret_cast<const uint4*>(J1.x);
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      const int nv = n / 8;
+      int v = tid;
+      uint4 q0 = z, q1 = z;
+      if (v < nv) {
+        if (J0.valid) q0 = x0[v];
+        if (J1.valid) q1 = x1[v];
+      }
+      for (int vw = tid * 8; vw < nv; vw += NT * 8) {  // one 128-byte line of each weight vector
+        if (J0.valid) asm volatile("prefetch.global.L2 [%0];" ::"l"(J0.w + 8 * vw));
+        if (J1.valid) asm volatile("prefetch.global.L2 [%0];" ::"l"(J1.w + 8 * vw));
+      }
+      auto sq = [](DF& acc, const uint4& q) {
+        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float a = bf16_lo(u[t]), b = bf16_hi(u[t]);
           df_add(acc, __fmul_rn(a, a));
+          df_add(acc, __fmul_rn(b, b));
+        }
+      };
+      while (v < nv) {
+        const int vn = v + NT;
+        uint4 n0 = z, n1 = z;
+        if (vn < nv) {
+          if (J0.valid) n0 = x0[vn];
+          if (J1.valid) n1 = x1[vn];
+        }
+        sq(acc0, q0);
+        sq(acc1, q1);
+        q0 = n0;
+        q1 = n1;
+        v = vn;
+      }
+    } else {
+      for (int k = tid; k < n; k += NT) {
+        if (J0.valid) {
+          const float a = bf16_bits_to_f32(J0.x[k]);
+          df_add(acc0, __fmul_rn(a, a));
+        }
+        if (J1.valid) {
+          const float a = bf16_bits_to_f32(J1.x[k]);
+          df_add(acc1, __fmul_rn(a, a));
         }
       }
     }
+    if (!called) {
+      after_loads();
+      called = true;
+    }
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1) acc = df_add(acc, shfl_xor_df(acc, m));
+    for (int m = 16; m > 0; m >>= 1) {
+      acc0 = df_add(acc0, shfl_xor_df(acc0, m));
+      acc1 = df_add(acc1, shfl_xor_df(acc1, m));
+    }
     if (lane == 0) {
-      red[(j * NW + warp) * 2] = acc.hi;
-      red[(j * NW + warp) * 2 + 1] = acc.lo;
+      red[(j0 * NW + warp) * 2] = acc0.hi;
+      red[(j0 * NW + warp) * 2 + 1] = acc0.lo;
+      if (j0 + 1 < njobs) {
+        red[((j0 + 1) * NW + warp) * 2] = acc1.hi;
+        red[((j0 + 1) * NW + warp) * 2 + 1] = acc1.lo;
+      }
     }
   }
+  if (!called) after_loads();
   __syncthreads();
   float* rr = red + njobs * NW * 2;
   for (int j = tid; j < njobs; j += NT) {
     DF tot{red[j * NW * 2], red[j * NW * 2 + 1]};
     for (int i = 1; i < NW; ++i) tot = df_add(tot, DF{red[(j * NW + i) * 2], red[(j * NW + i) * 2 + 1]});
-    const double ms = (static_cast<double>(tot.hi) + static_cast<double>(tot.lo)) / static_cast<double>(n);
-    const double r = 1.0 / sqrt(ms + static_cast<double>(eps));
+    // 1 / rms in fp64 (rsqrt: within an ulp or two of the correctly rounded value)
+    const double ms = (static_cast<double>(tot.hi) + static_cast<double>(tot.lo)) * inv_n;
+    const double r = rsqrt(ms + static_cast<double>(eps));
     const float rh = static_cast<float>(r);
     rr[2 * j] = rh;
     rr[2 * j + 1] = static_cast<float>(r - static_cast<double>(rh));

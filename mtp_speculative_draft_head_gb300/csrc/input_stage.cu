@@ -29,9 +29,9 @@ __device__ __forceinline__ bool token_ok(int32_t tok, int V) { return tok >= 0 &
 
 // Build c_b = [enorm(embed[tok_b]) | hnorm(hidden_b)] for sequences b0 .. b0+nb-1 into shared
 // memory (slot b - b0); valid[slot] says whether the token was in range.
-template <int NT>
+template <int NT, class AfterLoads = NoOp>
 __device__ void build_concat(const InputArgs& a, int b0, int nb, uint16_t* vec, int vec_elems,
-                             float* red, bool* valid) {
+                             float* red, bool* valid, AfterLoads after_loads = AfterLoads{}) {
   const int H = a.H;
   if (threadIdx.x < nb) {
     const bool ok = token_ok(a.tokens[b0 + threadIdx.x], a.V);
@@ -49,7 +49,7 @@ __device__ void build_concat(const InputArgs& a, int b0, int nb, uint16_t* vec, 
     }
     return NormJob{a.hidden + static_cast<size_t>(b) * H, a.hnorm_w, cb + H, true};
   };
-  rms_norm_multi_to_smem<NT>(2 * nb, H, a.eps, red, job, LayoutIdentity{});
+  rms_norm_multi_to_smem<NT>(2 * nb, H, a.inv_h, a.eps, red, job, LayoutIdentity{}, after_loads);
   __syncthreads();
 }
 
@@ -97,9 +97,20 @@ __global__ void __launch_bounds__(NWI * 32, 1) input_tma_kernel(const InputArgs 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t r0 = static_cast<int64_t>(H) * blockIdx.x / gridDim.x;
   const int64_t r1 = static_cast<int64_t>(H) * (blockIdx.x + 1) / gridDim.x;
-  const int64_t cta_rows = r1 - r0;
-  const int nrows = cta_rows > warp ? static_cast<int>((cta_rows - warp + NW - 1) / NW) : 0;
-  const int nitems = nrows * cpr;
+  const int cta_rows = static_cast<int>(r1 - r0);
+  // The CTA's work is cta_rows x cpr chunks of 4 KB (row-major, i.e. contiguous in memory).
+  // Warps take contiguous runs of equal length, so a row may be split between two warps (each
+  // run is at least a row long, so never among more). Whole rows per warp left 2 or 3 rows
+  // each at GLM size: the 3-row warps set the end. With fewer chunks than a row per warp the
+  // runs stay row-aligned.
+  const int F = cta_rows * cpr;
+  const bool by_chunk = F / NW >= cpr;
+  auto run_start = [&](int w) {
+    return by_chunk ? static_cast<int>(static_cast<int64_t>(F) * w / NW)
+                    : cpr * static_cast<int>(static_cast<int64_t>(cta_rows) * w / NW);
+  };
+  const int f0 = run_start(warp), f1 = run_start(warp + 1);
+  const int nitems = f1 - f0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NW * S; ++i) mbar_init(smem_addr(&bars[i]), 1);
@@ -111,43 +122,62 @@ __global__ void __launch_bounds__(NWI * 32, 1) input_tma_kernel(const InputArgs 
   uint64_t* my_bars = bars + warp * S;
   const uint64_t policy = l2_evict_first_policy();
   const uint8_t* W = reinterpret_cast<const uint8_t*>(a.eh_proj);
-  int pi = 0, pc = 0, ps = 0;
+  int pf = f0, ps = 0;
   auto issue_next = [&]() {
-    const int64_t row = r0 + warp + static_cast<int64_t>(pi) * NW;
+    const int64_t row = r0 + pf / cpr;
+    const int pc = pf % cpr;
     const uint32_t bytes = (pc == cpr - 1) ? last_bytes : static_cast<uint32_t>(kChunk);
     const uint8_t* src = W + row * row_bytes + static_cast<int64_t>(pc) * kChunk;
     const uint32_t bar = smem_addr(&my_bars[ps]);
     mbar_arrive_expect_tx(bar, bytes);
     bulk_copy_g2s(smem_addr(my_stages + static_cast<size_t>(ps) * kChunk), src, bytes, bar, policy);
-    if (++pc == cpr) { pc = 0; ++pi; }
+    ++pf;
     if (++ps == S) ps = 0;
   };
   const int prefill = nitems < S ? nitems : S;
-  if (lane == 0)
-    for (int t = 0; t < prefill; ++t) issue_next();
+  // The weight stages are issued once the prologue has read the embedding row and
+  // target_hidden: issued first, the weight stages of all SMs (~30 MB) sat in front of those
+  // reads in the memory queues and delayed the prologue by several us.
 
   // tokens and target_hidden may come from the preceding kernel
   pdl_wait_prior_grid();
-  build_concat<NW * 32>(a, 0, NB, vec, vec_elems, red, valid_s);
+  auto start_weights = [&]() {
+    if (lane == 0)
+      for (int t = 0; t < prefill; ++t) issue_next();
+  };
+  build_concat<NW * 32>(a, 0, NB, vec, vec_elems, red, valid_s, start_weights);
   bool valid[NB];
 #pragma unroll
   for (int b = 0; b < NB; ++b) valid[b] = valid_s[b];
   pdl_launch_dependents();
 
+  // partial sums of rows split between two warps: [warp][first | last][sequence]
+  DF* part = reinterpret_cast<DF*>(red);
   const uint64_t zero2 = f2_pack(0.0f, 0.0f);
   DF2 acc[NB][4];
 #pragma unroll
   for (int b = 0; b < NB; ++b)
 #pragma unroll
     for (int u = 0; u < 4; ++u) acc[b][u] = DF2{zero2, zero2};
-  int ci = 0, cc = 0, cs = 0, t_fail = -1;
+  int cs = 0, t_fail = -1;
   uint32_t parity = 0;
+  auto row_total = [&](int b) {
+    DF v = df_add(df_add(df_add(df2_x(acc[b][0]), df2_y(acc[b][0])), df_add(df2_x(acc[b][1]), df2_y(acc[b][1]))),
+                  df_add(df_add(df2_x(acc[b][2]), df2_y(acc[b][2])), df_add(df2_x(acc[b][3]), df2_y(acc[b][3]))));
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v = df_add(v, shfl_xor_df(v, m));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[b][u] = DF2{zero2, zero2};
+    return v;
+  };
   for (int t = 0; t < nitems; ++t) {
     const uint32_t bar = smem_addr(&my_bars[cs]);
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar, parity))) {
       t_fail = t;
       break;
     }
+    const int f = f0 + t;
+    const int cc = f % cpr;
     const uint4* wv = reinterpret_cast<const uint4*>(my_stages + static_cast<size_t>(cs) * kChunk);
     const int nv = static_cast<int>(((cc == cpr - 1) ? last_bytes : static_cast<uint32_t>(kChunk)) >> 4);
     const int J0 = cc * (kChunk / 16);
@@ -166,30 +196,45 @@ __global__ void __launch_bounds__(NWI * 32, 1) input_tma_kernel(const InputArgs 
       issue_next();
     }
     if (++cs == S) { cs = 0; parity ^= 1u; }
-    if (++cc == cpr) {
-      const int64_t row = r0 + warp + static_cast<int64_t>(ci) * NW;
-      cc = 0;
-      ++ci;
+    if (cc == cpr - 1 || t == nitems - 1) {
+      // end of a row, or of this warp's run in the middle of one
+      const int rl = f / cpr;
+      const bool whole = rl * cpr >= f0 && cc == cpr - 1;
+      const int slot = (cc == cpr - 1) ? 0 : 1;  // row finished here: its start was the previous warp's
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        DF v = df_add(df_add(df_add(df2_x(acc[b][0]), df2_y(acc[b][0])), df_add(df2_x(acc[b][1]), df2_y(acc[b][1]))),
-                      df_add(df_add(df2_x(acc[b][2]), df2_y(acc[b][2])), df_add(df2_x(acc[b][3]), df2_y(acc[b][3]))));
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) v = df_add(v, shfl_xor_df(v, m));
-        if (lane == 0) a.x[static_cast<size_t>(b) * H + row] = valid[b] ? bf16_rne_df(v.hi, v.lo) : uint16_t(0);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) acc[b][u] = DF2{zero2, zero2};
+        const DF v = row_total(b);
+        if (lane == 0) {
+          if (whole) a.x[static_cast<size_t>(b) * H + r0 + rl] = valid[b] ? bf16_rne_df(v.hi, v.lo) : uint16_t(0);
+          else part[(warp * 2 + slot) * NB + b] = v;
+        }
       }
     }
   }
   if (t_fail >= 0 && lane == 0) {
     store_status(a.status, MTP_ERR_TIMEOUT);
     // let the copies still in flight land before the CTA's shared memory is released
-    int s = cs;
+    int s2 = cs;
     uint32_t par = parity;
     for (int u = t_fail; u < nitems && u < t_fail + S; ++u) {
-      (void)mbar_wait_bounded(smem_addr(&my_bars[s]), par);
-      if (++s == S) { s = 0; par ^= 1u; }
+      (void)mbar_wait_bounded(smem_addr(&my_bars[s2]), par);
+      if (++s2 == S) { s2 = 0; par ^= 1u; }
+    }
+  }
+  if (by_chunk) {
+    // rows split at a warp boundary: the earlier warp's part (its "last") plus the later one's
+    // ("first"), in that order
+    __syncthreads();
+    if (t_fail < 0 && threadIdx.x >= 1 && threadIdx.x < NW) {
+      const int w = threadIdx.x, fb = run_start(w);
+      if (fb % cpr != 0) {
+        const int rl = fb / cpr;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const DF v = df_add(part[((w - 1) * 2 + 1) * NB + b], part[(w * 2 + 0) * NB + b]);
+          a.x[static_cast<size_t>(b) * H + r0 + rl] = valid_s[b] ? bf16_rne_df(v.hi, v.lo) : uint16_t(0);
+        }
+      }
     }
   }
 }

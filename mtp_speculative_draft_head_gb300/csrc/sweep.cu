@@ -221,7 +221,7 @@ __device__ void final_norm_prologue(const SweepArgs& a, int nb, uint16_t* vec, i
     return NormJob{a.x + static_cast<size_t>(b) * a.H, a.final_norm_w,
                    vec + static_cast<size_t>(b) * vec_elems, true};
   };
-  rms_norm_multi_to_smem<NT>(nb, a.H, a.eps, red, job, Layout{});
+  rms_norm_multi_to_smem<NT>(nb, a.H, a.inv_h, a.eps, red, job, Layout{});
   __syncthreads();
 }
 
