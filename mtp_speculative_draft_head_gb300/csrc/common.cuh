@@ -19,6 +19,7 @@ namespace mtp {
 constexpr int kMaxB = 16;        // sequences per sweep
 constexpr int kMaxGrid = 1024;   // CTAs per launch (bounds the workspace)
 constexpr int kWsHeader = 128;   // workspace bytes before the per-CTA partials
+constexpr int kRowCounterOffset = 64;  // header word: next dynamically claimed row
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // give up a wait after 2 s
 
 // ------------------------------------------------------------------------------------------

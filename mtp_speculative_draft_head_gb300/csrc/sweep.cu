@@ -71,7 +71,11 @@ __device__ void argmax_finish(const ArgBest* best, int nb, ArgBest* wbest, uint8
   if (is_last) {
     __threadfence();
     combine_partials(part, gridDim.x, nb, draft);
-    if (threadIdx.x == 0) atomicExch(counter, 0u);
+    if (threadIdx.x == 0) {
+      // every CTA has finished claiming rows: ready for the next launch
+      atomicExch(reinterpret_cast<unsigned int*>(ws + kRowCounterOffset), 0u);
+      atomicExch(counter, 0u);
+    }
   }
 }
 
@@ -256,10 +260,26 @@ __global__ void __launch_bounds__(NWR * 32, 1) sweep_regx_kernel(const SweepArgs
   ArgBest* wbest = reinterpret_cast<ArgBest*>(red + kRedBytes / sizeof(float));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t r0 = V * blockIdx.x / gridDim.x;
-  const int64_t r1 = V * (blockIdx.x + 1) / gridDim.x;
-  const int64_t cta_rows = r1 - r0;
-  const int nrows = cta_rows > warp ? static_cast<int>((cta_rows - warp + NWR - 1) / NWR) : 0;
+  // per-warp queues: row and row scale of each stage, row and scale of each group slot
+  int* rowq = reinterpret_cast<int*>(wbest + kWarps * kMaxB) + warp * (2 * kMaxStages + 2 * kGroup);
+  float* scq = reinterpret_cast<float*>(rowq + kMaxStages);
+  int* grow = rowq + 2 * kMaxStages;
+  float* gsc = reinterpret_cast<float*>(grow + kGroup);
+  // Rows are handed out dynamically: each warp's first S rows are fixed (they are prefetched
+  // before the preceding kernel has finished), the rest are claimed kClaim at a time from a
+  // counter in the workspace header. With a fixed split, CTAs ended their last rows up to
+  // ~60 us apart (some SMs draw less bandwidth) and the kernel waited for the slowest.
+  constexpr int kClaim = (WT == MTP_W_BF16) ? 4 : 8;  // ~48 KB of weights per claim
+  unsigned int* row_counter = reinterpret_cast<unsigned int*>(a.ws + kRowCounterOffset);
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * NWR + warp;
+  const int64_t nstatic = V < static_cast<int64_t>(gridDim.x) * NWR * S ? V : static_cast<int64_t>(gridDim.x) * NWR * S;
+  // issue side, lane 0 only: current block [cur, cur_end) and the block claimed ahead
+  int64_t cur = gw * S, cur_end = cur + S < V ? cur + S : V;
+  unsigned int nxt = 0;
+  bool have_nxt = false, exhausted = false;
+  int issued = 0;
+  float pend_scale = 1.0f;
+  int pend_stage = -1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NWR * S; ++i) mbar_init(smem_addr(&bars[i]), 1);
@@ -270,20 +290,52 @@ __global__ void __launch_bounds__(NWR * 32, 1) sweep_regx_kernel(const SweepArgs
   uint8_t* my_stages = stages + static_cast<size_t>(warp) * S * RB;
   uint64_t* my_bars = bars + warp * S;
   const uint64_t policy = l2_evict_first_policy();
-  int pi = 0, ps = 0;
-  auto issue_next = [&]() {
-    const int64_t row = r0 + warp + static_cast<int64_t>(pi) * NWR;
+  int ps = 0;
+  auto issue_next = [&]() {  // lane 0
+    if (cur >= cur_end) {
+      if (!have_nxt) {
+        exhausted = true;
+        return;
+      }
+      cur = nstatic + static_cast<int64_t>(nxt);
+      cur_end = cur + kClaim < V ? cur + kClaim : V;
+      if (cur >= V) {
+        exhausted = true;
+        have_nxt = false;
+        return;
+      }
+      nxt = atomicAdd(row_counter, static_cast<unsigned int>(kClaim));  // the one after, ahead of need
+    }
+    const int64_t row = cur++;
     const uint32_t bar = smem_addr(&my_bars[ps]);
     mbar_arrive_expect_tx(bar, RB);
     bulk_copy_g2s(smem_addr(my_stages + static_cast<size_t>(ps) * RB), a.W + row * RB, RB, bar, policy);
-    ++pi;
+    rowq[ps] = static_cast<int>(row);
+    if constexpr (WT == MTP_W_FP8_E4M3) {
+      // the scale load is stored one issue later, when it has long arrived
+      if (pend_stage >= 0) scq[pend_stage] = pend_scale;
+      pend_scale = __ldg(a.scale + row);
+      pend_stage = ps;
+    }
+    ++issued;
     if (++ps == S) ps = 0;
   };
-  const int prefill = nrows < S ? nrows : S;
-  if (lane == 0)
-    for (int t = 0; t < prefill; ++t) issue_next();
+  auto flush_scale = [&]() {  // lane 0
+    if constexpr (WT == MTP_W_FP8_E4M3) {
+      if (pend_stage >= 0) scq[pend_stage] = pend_scale;
+      pend_stage = -1;
+    }
+  };
+  if (lane == 0) {
+    for (int t = 0; t < S && !exhausted; ++t) issue_next();
+    if (exhausted) flush_scale();  // only when V leaves nothing to claim
+  }
 
-  pdl_wait_prior_grid();  // x comes from the preceding kernel
+  pdl_wait_prior_grid();  // x comes from the preceding kernel; the row counter is free again
+  if (lane == 0 && nstatic < V) {
+    nxt = atomicAdd(row_counter, static_cast<unsigned int>(kClaim));
+    have_nxt = true;
+  }
   final_norm_prologue<NWR * 32, XhatLayout<WT>>(a, 1, vec, H, red);
   float unscale = 1.0f;  // 2^-k for the f16 activations
   float xscale = 1.0f;   // 2^k
@@ -331,25 +383,14 @@ __global__ void __launch_bounds__(NWR * 32, 1) sweep_regx_kernel(const SweepArgs
   float part[kGroup];
 #pragma unroll
   for (int j = 0; j < kGroup; ++j) part[j] = 0.0f;
-  int cs = 0, i_fail = -1;
+  int cs = 0, i_fail = -1, consumed = 0;
   uint32_t parity = 0;
-  // row scales of this lane's slot, loaded one group ahead so the load is off the critical path
-  float my_scale = 1.0f, next_scale = 1.0f;
-  if constexpr (WT == MTP_W_FP8_E4M3) {
-    if (my_slot < nrows) next_scale = __ldg(a.scale + r0 + warp + static_cast<int64_t>(my_slot) * NWR);
-  }
+  int n_issued = __shfl_sync(0xffffffffu, issued, 0);
 #pragma unroll 1
-  for (int i = 0; i < nrows; ++i) {
-    const int jj = i & (kGroup - 1);
-    if constexpr (WT == MTP_W_FP8_E4M3) {
-      if (jj == 0) {
-        my_scale = next_scale;
-        const int nxt = i + kGroup + my_slot;
-        if (nxt < nrows) next_scale = __ldg(a.scale + r0 + warp + static_cast<int64_t>(nxt) * NWR);
-      }
-    }
+  while (consumed < n_issued) {
+    const int jj = consumed & (kGroup - 1);
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&my_bars[cs]), parity))) {
-      i_fail = i;
+      i_fail = consumed;
       break;
     }
     const uint4* wv = reinterpret_cast<const uint4*>(my_stages + static_cast<size_t>(cs) * RB);
@@ -371,33 +412,44 @@ __global__ void __launch_bounds__(NWR * 32, 1) sweep_regx_kernel(const SweepArgs
     const float pv = __fadd_rn(acc0, acc1);
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) part[j] = (j == jj) ? pv : part[j];
+    if (lane == 0) {
+      grow[jj] = rowq[cs];
+      if constexpr (WT == MTP_W_FP8_E4M3) gsc[jj] = scq[cs];
+    }
     __syncwarp();
-    if (lane == 0 && i + S < nrows) {
+    ++consumed;
+    if (lane == 0 && !exhausted) {
       fence_proxy_async_smem();
       issue_next();
+      if (exhausted) flush_scale();
     }
+    n_issued = __shfl_sync(0xffffffffu, issued, 0);
     if (++cs == S) { cs = 0; parity ^= 1u; }
-    if (jj == kGroup - 1 || i == nrows - 1) {
+    if (jj == kGroup - 1 || consumed == n_issued) {
+      __syncwarp();
       float v = transpose_reduce8(part, lane);
-      if constexpr (kF16) v = __fmul_rn(__fmul_rn(v, unscale), my_scale);
-      else if constexpr (WT == MTP_W_FP8_E4M3) v = __fmul_rn(__fmul_rn(v, kE4m3Unscale), my_scale);
       if (my_slot <= jj) {
-        const int64_t my_row = r0 + warp + static_cast<int64_t>(i - jj + my_slot) * NWR;
+        const int my_row = grow[my_slot];
+        if constexpr (kF16) v = __fmul_rn(__fmul_rn(v, unscale), gsc[my_slot]);
+        else if constexpr (WT == MTP_W_FP8_E4M3) v = __fmul_rn(__fmul_rn(v, kE4m3Unscale), gsc[my_slot]);
         if ((lane & 3) == 0 && a.logits != nullptr) a.logits[my_row] = v;
         arg_update(best, v, static_cast<int32_t>(my_row));
       }
 #pragma unroll
       for (int j = 0; j < kGroup; ++j) part[j] = 0.0f;
+      __syncwarp();
     }
   }
-  if (i_fail >= 0 && lane == 0) {
-    store_status(a.status, MTP_ERR_TIMEOUT);
-    // let the copies still in flight land before the CTA's shared memory is released
-    int s = cs;
-    uint32_t par = parity;
-    for (int u = i_fail; u < nrows && u < i_fail + S; ++u) {
-      (void)mbar_wait_bounded(smem_addr(&my_bars[s]), par);
-      if (++s == S) { s = 0; par ^= 1u; }
+  if (i_fail >= 0) {
+    if (lane == 0) {
+      store_status(a.status, MTP_ERR_TIMEOUT);
+      // let the copies still in flight land before the CTA's shared memory is released
+      int s2 = cs;
+      uint32_t par = parity;
+      for (int u = i_fail; u < n_issued && u < i_fail + S; ++u) {
+        (void)mbar_wait_bounded(smem_addr(&my_bars[s2]), par);
+        if (++s2 == S) { s2 = 0; par ^= 1u; }
+      }
     }
   }
   __syncwarp();
@@ -593,7 +645,9 @@ cudaError_t launch_sweep_kernel(void (*kernel)(SweepArgs), unsigned grid, unsign
 }
 
 constexpr bool kMixedDefault = MTP_MIXED_FMA != 0;
-constexpr size_t kMisc = kRedBytes + static_cast<size_t>(kWarps) * kMaxB * sizeof(ArgBest) + 256;
+// per-warp row queues of the single-sequence kernel (up to 16 warps)
+constexpr size_t kQueueBytes = static_cast<size_t>(16) * (2 * kMaxStages + 2 * kGroup) * 4;
+constexpr size_t kMisc = kRedBytes + static_cast<size_t>(kWarps) * kMaxB * sizeof(ArgBest) + kQueueBytes + 256;
 
 template <int WT, int NB>
 cudaError_t launch_tma(SweepArgs a, const DeviceInfo& di, unsigned grid, size_t fixed, cudaStream_t stream) {

@@ -83,7 +83,10 @@ SHAPES = [  # (H, V, B): tiles, ragged tails and every path
     (1000, 5003, 3),    # B >= 2, H % 8 == 0 -> tensor-core kernel (partial last k-block)
     (2056, 1031, 2),    # tensor-core kernel, ragged last row tile
     (2048, 777, 4),
-    (6144, 1000, 1),    # GLM hidden size: 3 BF16 chunks, FP8 one full + one partial chunk
+    (6144, 1000, 1),    # GLM hidden size: 3 BF16 chunks, FP8 one full + one partial chunk;
+                        # V below the rows fixed per warp (no dynamic hand-out)
+    (4096, 3650, 1),    # a few rows past the fixed ones (BF16): dynamic blocks, a partial last one
+    (4096, 7300, 1),    # the same for FP8 (12 warps, more fixed rows)
     (4096, 300, 5),
     (512, 2000, 16),    # B = 16: two n-tiles of 8 sequences
     (544, 160000, 9),   # output: more than 8 row tiles per CTA; input: a k-chunk across the
