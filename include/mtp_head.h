@@ -95,6 +95,38 @@ int mtp_head_input(const uint16_t* embed, const uint16_t* enorm_w, const uint16_
                    uint16_t* x_out, int32_t* status, int H, int V, float eps, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Context-row input stage ("glm5next_mtp_head.rs", `rows_impl`: for every context row r, the
+ * embedding row of tokens[r] and target_hidden row r go through enorm / hnorm, the concat and
+ * eh_proj -- the input stage of `forward_one` per row; the source loops over the rows on the
+ * host, here all R rows run at once).
+ *
+ *   embed, enorm_w, hnorm_w, eh_proj  as for mtp_head_input_batched
+ *   tokens         [R]     int32  device-resident tokens; tokens[r] is the token row r pairs
+ *                                 with (the source pairs hidden row r with the token after it,
+ *                                 so a caller passes its token array shifted by one)
+ *   target_hidden  [R, H]  BF16
+ *   x_out          [R, H]  BF16   output; a row whose token is outside [0, V) is zeros and
+ *                                 status (optional) gets MTP_ERR_TOKEN_RANGE
+ *   workspace             device scratch of at least mtp_head_context_workspace_bytes(R, H)
+ *                         bytes (no initialisation needed; may be NULL when R <= 16)
+ *   R              1 .. 65536 rows
+ *
+ * R <= 16 runs the batched input stage (one pass over eh_proj for all rows). Larger R runs two
+ * kernels: the normalised concat of every row into the workspace (the same correctly rounded
+ * BF16 values as the input stage), then x = concat . eh_proj^T as a tiled GEMM on the
+ * tcgen05 tensor cores with FP32 accumulation -- the source's eh_proj precision, so x is the
+ * BF16 rounding of an FP32-accumulated sum. H must be a multiple of 32 for R > 16
+ * (MTP_ERR_NOT_IMPLEMENTED otherwise).
+ * ---------------------------------------------------------------------------------------- */
+int mtp_head_context_rows(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hnorm_w,
+                          const uint16_t* eh_proj, const int32_t* tokens, const uint16_t* target_hidden,
+                          uint16_t* x_out, int32_t* status, void* workspace, size_t workspace_bytes,
+                          int R, int H, int V, float eps, void* stream);
+
+/* Bytes of workspace mtp_head_context_rows needs for R rows (0 for invalid shapes). */
+size_t mtp_head_context_workspace_bytes(int R, int H);
+
+/* ------------------------------------------------------------------------------------------
  * Output stage ("glm5next_mtp_head.rs", `forward_one`: `shared_head.norm` in place, then the
  * `lm_head` dense gemv -- or `dense_gemv_fp8w` over the FP8 copy described in the `head_fp8`
  * doc -- then `argmax_bf16`; here the sweep covers the whole vocabulary on one GPU and the

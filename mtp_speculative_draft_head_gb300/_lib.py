@@ -42,6 +42,8 @@ SIGNATURES = {
     "mtp_head_forward_batched": (I, [P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, Z, I, I, I, F, P]),
     "mtp_head_forward_host": (I, [P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, P, P, Z, I, I, I, F, P]),
     "mtp_head_quantize_fp8": (I, [P, P, P, P, I, I, P]),
+    "mtp_head_context_rows": (I, [P, P, P, P, P, P, P, P, P, Z, I, I, I, F, P]),
+    "mtp_head_context_workspace_bytes": (Z, [I, I]),
     "mtp_head_strerror": (ctypes.c_char_p, [I]),
 }
 
@@ -127,6 +129,30 @@ def mtp_head_input_batched(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidd
         _dev(eh_proj, "eh_proj"), _dev(tokens, "tokens"), _dev(target_hidden, "target_hidden"),
         _dev(x_out, "x_out"), _dev(status, "status"), B, H, V, eps, _stream(stream)),
         "mtp_head_input_batched")
+
+
+def mtp_head_context_workspace_bytes(R: int, H: int) -> int:
+    return int(load().mtp_head_context_workspace_bytes(R, H))
+
+
+def context_workspace(R: int, H: int, device=None) -> torch.Tensor:
+    """Scratch for mtp_head_context_rows (no initialisation needed)."""
+    n = mtp_head_context_workspace_bytes(R, H)
+    if n == 0:
+        raise MTPError(ERR_SHAPE, "context_workspace")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def mtp_head_context_rows(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidden, x_out, ws=None,
+                          status=None, eps: float = 1e-6, stream=None) -> None:
+    V, H = embed.shape
+    R = tokens.numel()
+    _check(load().mtp_head_context_rows(
+        _dev(embed, "embed"), _dev(enorm_w, "enorm_w"), _dev(hnorm_w, "hnorm_w"),
+        _dev(eh_proj, "eh_proj"), _dev(tokens, "tokens"), _dev(target_hidden, "target_hidden"),
+        _dev(x_out, "x_out"), _dev(status, "status"), _dev(ws, "workspace"),
+        0 if ws is None else ws.numel() * ws.element_size(), R, H, V, eps, _stream(stream)),
+        "mtp_head_context_rows")
 
 
 def mtp_head_input(embed, enorm_w, hnorm_w, eh_proj, token, target_hidden, x_out, status=None,

@@ -12,6 +12,7 @@
 namespace {
 
 using mtp::kMaxB;
+constexpr int kMaxContextRows = 65536;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -214,6 +215,47 @@ int mtp_head_forward_host(const uint16_t* embed, const uint16_t* enorm_w, const 
     return MTP_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MTP_ERR_CUDA;
   return dev_status;
+}
+
+size_t mtp_head_context_workspace_bytes(int R, int H) {
+  if (R < 1 || R > kMaxContextRows || H < 1 || H > 65536) return 0;
+  return mtp::context_workspace_bytes(R, H);
+}
+
+int mtp_head_context_rows(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hnorm_w,
+                          const uint16_t* eh_proj, const int32_t* tokens, const uint16_t* target_hidden,
+                          uint16_t* x_out, int32_t* status, void* workspace, size_t workspace_bytes, int R,
+                          int H, int V, float eps, void* stream) {
+  if (!embed || !enorm_w || !hnorm_w || !eh_proj || !tokens || !target_hidden || !x_out) return MTP_ERR_ARG;
+  if (check_eps(eps) != MTP_OK) return MTP_ERR_ARG;
+  if (R < 1 || R > kMaxContextRows || H < 1 || H > 65536 || V < 1) return MTP_ERR_SHAPE;
+  if (!aligned(embed, 16) || !aligned(enorm_w, 16) || !aligned(hnorm_w, 16) || !aligned(eh_proj, 16) ||
+      !aligned(target_hidden, 16) || !aligned(x_out, 16) || !aligned(tokens, 4) ||
+      (status && !aligned(status, 4)) || (workspace && !aligned(workspace, 16)))
+    return MTP_ERR_ALIGN;
+  if (R <= kMaxB)  // a few rows: the batched input stage, one weight pass for all of them
+    return run_input(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidden, x_out, status, R, H, V, eps,
+                     stream);
+  if (H % 32 != 0) return MTP_ERR_NOT_IMPLEMENTED;
+  if (!workspace || workspace_bytes < mtp::context_workspace_bytes(R, H)) return MTP_ERR_WORKSPACE;
+  mtp::ContextArgs a{};
+  a.embed = embed;
+  a.enorm_w = enorm_w;
+  a.hnorm_w = hnorm_w;
+  a.eh_proj = eh_proj;
+  a.tokens = tokens;
+  a.hidden = target_hidden;
+  a.x = x_out;
+  a.status = status;
+  a.concat = static_cast<uint16_t*>(workspace);
+  a.valid = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
+                                       (static_cast<size_t>(R) * 2 * H * 2 + 255) / 256 * 256);
+  a.R = R;
+  a.H = H;
+  a.V = V;
+  a.eps = eps;
+  a.inv_h = 1.0 / static_cast<double>(H);
+  return map_cuda(mtp::launch_context_rows(a, static_cast<cudaStream_t>(stream)));
 }
 
 int mtp_head_quantize_fp8(const uint16_t* w, uint8_t* q, float* row_scale, int32_t* status, int V,

@@ -90,6 +90,26 @@ struct SweepArgs {
   int stages;
 };
 
+struct ContextArgs {
+  const uint16_t* embed;
+  const uint16_t* enorm_w;
+  const uint16_t* hnorm_w;
+  const uint16_t* eh_proj;
+  const int32_t* tokens;
+  const uint16_t* hidden;
+  uint16_t* x;
+  int32_t* status;
+  uint16_t* concat;  // workspace: [R, 2H] BF16
+  int32_t* valid;    // workspace: [R] token-in-range flags
+  int R, H, V;
+  float eps;
+  double inv_h;
+};
+
+// Context rows (R >= 1, H a multiple of 32): concat kernel + tensor-core GEMM.
+cudaError_t launch_context_rows(const ContextArgs& a, cudaStream_t stream);
+size_t context_workspace_bytes(int R, int H);
+
 cudaError_t launch_input_stage(const InputArgs& a, cudaStream_t stream);
 // Batched (2 <= B <= 16) input stage on tensor cores; *launched stays false when the shape is
 // not supported (H not a multiple of 8, not enough shared memory).

@@ -1,0 +1,155 @@
+"""GPU parity of the context-row input stage (mtp_head_context_rows) against the CPU oracle.
+
+For R > 16 rows the library runs two kernels: the normalised concat of every row (checked here
+bit for bit against the oracle's concat, read back from the workspace) and x = concat . eh_proj^T
+on the tensor cores with FP32 accumulation (checked against the oracle's fp64 sum within the
+FP32-accumulation band below, plus a bound on how many elements may differ from the correctly
+rounded x at all). R <= 16 must give exactly what the batched input stage gives.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mtp_speculative_draft_head_gb300 as m
+import oracle
+import synth
+from gpu_helpers import abs_product_sums, check_x
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+EPS = synth.EPS
+
+
+def context_band(K: int) -> float:
+    """Relative band (times sum_k |p_k|) of an FP32 accumulation of K exact BF16 products on the
+    tensor cores: the MMAs add K / 16 groups of 16 exact products into the FP32 accumulator, and
+    each of those additions (with whatever internal alignment the hardware uses inside a group)
+    is taken to err by at most 2^-22 of the sum of |products| accumulated so far."""
+    return (K / 16 + 2) * 2.0 ** -22
+
+
+class Ctx:
+    def __init__(self, H, R, V=4096, seed=0, tokens=None):
+        self.H, self.R, self.V = H, R, V
+        w = synth.make_weights(H, V, seed, "cpu")
+        t, self.hidden = synth.make_step_inputs(H, V, R, seed + 7, "cpu", distinct=False)
+        self.tokens = t if tokens is None else tokens
+        self.wb = {k: synth.bits(v) for k, v in w.as_dict().items()}
+        self.g = {k: v.to(DEV) for k, v in w.as_dict().items()}
+
+    def run(self, ws_extra=0):
+        x = torch.full((self.R, self.H), 7, dtype=torch.bfloat16, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        n = m.mtp_head_context_workspace_bytes(self.R, self.H)
+        ws = torch.empty(n + ws_extra, dtype=torch.uint8, device=DEV) if n else None
+        m.mtp_head_context_rows(self.g["embed"], self.g["enorm_w"], self.g["hnorm_w"], self.g["eh_proj"],
+                                self.tokens.to(DEV), self.hidden.to(DEV), x, ws, st, EPS)
+        torch.cuda.synchronize()
+        return synth.bits(x), int(st.item()), ws
+
+    def oracle(self, rows=None):
+        rows = np.arange(self.R) if rows is None else np.asarray(rows)
+        tok = synth.bits(self.tokens).astype(np.int64)[rows]
+        hid = synth.bits(self.hidden)[rows]
+        x, concat, st, sums = oracle.input_stage(self.wb["embed"], self.wb["enorm_w"], self.wb["hnorm_w"],
+                                                 self.wb["eh_proj"], tok, hid, EPS, return_concat=True,
+                                                 return_sums=True)
+        return x, concat, st, sums
+
+
+def workspace_concat(ws, R, H):
+    """The normalised concat rows the first kernel leaves at the start of the workspace."""
+    return ws[: R * 2 * H * 2].view(torch.int16).view(R, 2 * H).cpu().numpy().view(np.uint16)
+
+
+def check_rows(c, x_gpu, ws, rows=None):
+    rows = np.arange(c.R) if rows is None else np.asarray(rows)
+    x_ref, concat_ref, st_ref, sums = c.oracle(rows)
+    ok = st_ref == 0
+    assert np.array_equal(workspace_concat(ws, c.R, c.H)[rows][ok], concat_ref[ok]), "concat differs from the oracle"
+    abs_sums = abs_product_sums(c.wb["eh_proj"], concat_ref)
+    K = 2 * c.H
+    x_sel = x_gpu[rows]
+    assert np.all(x_sel[~ok] == 0), "rows with an out-of-range token must be zeros"
+    diff = np.nonzero(x_sel[ok] != x_ref[ok])[0].size
+    # the FP32-accumulation band, as an interval check around the exact sum
+    E = context_band(K) * abs_sums[ok]
+    g = oracle.bf16_to_f64(x_sel[ok])
+    s = sums[ok]
+    lo = oracle.bf16_to_f64(oracle.f64_to_bf16(s - E))
+    hi = oracle.bf16_to_f64(oracle.f64_to_bf16(s + E))
+    bad = ~((lo <= g) & (g <= hi))
+    assert not bad.any(), f"{int(bad.sum())} elements outside the FP32-accumulation band"
+    # a systematic error inside the worst-case band would still move many roundings
+    assert diff <= max(4, x_sel[ok].size // 100), f"{diff} of {x_sel[ok].size} elements differ from the oracle"
+    return diff
+
+
+@pytest.mark.parametrize("H,R", [
+    (256, 17),     # one row tile, one column tile, 8 k-blocks
+    (256, 300),    # three row tiles, ragged last one
+    (1024, 130),   # four column tiles, two row tiles (the second holds 2 rows)
+    (288, 200),    # H not a multiple of the 256-column tile: ragged last column tile
+    (96, 40),      # H below one column tile, 3 k-blocks (fewer than the ring's stages)
+    (2048, 257),
+])
+def test_context_rows_match_oracle(H, R):
+    c = Ctx(H, R, seed=H + R)
+    x, st, ws = c.run()
+    assert st == 0
+    check_rows(c, x, ws)
+
+
+def test_context_rows_glm_size_sampled():
+    """GLM hidden size, 512 context rows (the launch the benchmark times); oracle on sampled rows
+    at both ends of each row tile."""
+    c = Ctx(6144, 512, seed=11)
+    x, st, ws = c.run()
+    assert st == 0
+    check_rows(c, x, ws, rows=[0, 1, 127, 128, 300, 383, 384, 511])
+
+
+def test_context_rows_out_of_range_tokens():
+    H, R, V = 512, 150, 1000
+    c = Ctx(H, R, V=V, seed=3)
+    t = c.tokens.clone()
+    t[[0, 77, 128, 149]] = torch.tensor([-1, V, 2 ** 31 - 1, -(2 ** 31)], dtype=torch.int32)
+    c.tokens = t
+    x, st, ws = c.run()
+    assert st == m.ERR_TOKEN_RANGE
+    check_rows(c, x, ws)
+
+
+def test_context_rows_small_r_is_batched_input():
+    """R <= 16 runs the batched input stage: identical to mtp_head_input_batched, no workspace."""
+    H, R = 1024, 9
+    c = Ctx(H, R, seed=5)
+    x, st, _ = c.run()
+    assert st == 0
+    xb = torch.full((R, H), 7, dtype=torch.bfloat16, device=DEV)
+    stb = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.mtp_head_input_batched(c.g["embed"], c.g["enorm_w"], c.g["hnorm_w"], c.g["eh_proj"], c.tokens.to(DEV),
+                             c.hidden.to(DEV), xb, stb, EPS)
+    torch.cuda.synchronize()
+    assert np.array_equal(x, synth.bits(xb))
+
+
+def test_context_rows_deterministic_and_workspace_checked():
+    c = Ctx(512, 200, seed=9)
+    x1, _, _ = c.run()
+    x2, _, _ = c.run(ws_extra=4096)
+    assert np.array_equal(x1, x2)
+    small = torch.empty(m.mtp_head_context_workspace_bytes(200, 512) - 1, dtype=torch.uint8, device=DEV)
+    x = torch.empty((200, 512), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(m.MTPError) as e:
+        m.mtp_head_context_rows(c.g["embed"], c.g["enorm_w"], c.g["hnorm_w"], c.g["eh_proj"], c.tokens.to(DEV),
+                                c.hidden.to(DEV), x, small)
+    assert e.value.code == m.ERR_WORKSPACE
+    with pytest.raises(m.MTPError) as e:  # H % 32 != 0 with R > 16
+        c2 = Ctx(100, 20, seed=1)
+        x = torch.empty((20, 100), dtype=torch.bfloat16, device=DEV)
+        ws = torch.empty(m.mtp_head_context_workspace_bytes(20, 100), dtype=torch.uint8, device=DEV)
+        m.mtp_head_context_rows(c2.g["embed"], c2.g["enorm_w"], c2.g["hnorm_w"], c2.g["eh_proj"],
+                                c2.tokens.to(DEV), c2.hidden.to(DEV), x, ws)
+    assert e.value.code == m.ERR_NOT_IMPLEMENTED
