@@ -41,10 +41,12 @@ import synth  # noqa: E402
 METRIC = "lm_head draft sweep µs and HBM GB/s (BF16/FP8, H=6144, V=154880, B=1)"
 H, V, B = 6144, 154880, 1
 BATCHES = (2, 4, 8, 16)
+CONTEXT_ROWS = (512, 4096)  # context-row (prefill) batches timed through mtp_head_context_rows
 EPS = synth.EPS
 CHAIN = 1000
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sweep_traffic.json")
 SWEEP_SOURCES = [os.path.join(ROOT, "mtp_speculative_draft_head_gb300", "csrc", f)
                  for f in ("sweep.cu", "common.cuh", "internal.h")]
@@ -166,6 +168,14 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
 
 
+def peak_bf16():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s, one earlier GB300 measurement)"
+
+
 def sweep_source_sha() -> str:
     h = hashlib.sha256()
     for p in SWEEP_SOURCES:
@@ -236,9 +246,10 @@ def run_ours(args, world, rank, local):
                                            None, tok[i + 1], head.ws, status, EPS, st)
         return fn
 
+    d = torch.empty(1, dtype=torch.int32, device=dev)
+
     def sweep_fn(n, fp8):
         Wt, s, wt = head._head(fp8)
-        d = torch.empty(1, dtype=torch.int32, device=dev)
 
         def fn(st):
             for _ in range(n):
@@ -255,6 +266,7 @@ def run_ours(args, world, rank, local):
 
     results = {}
     tok[0].copy_(first)
+    stream.wait_stream(torch.cuda.current_stream())  # inputs were drawn on the current stream
     with torch.cuda.stream(stream):
         # warm-up: W eager steps of each kind
         for fp8 in (False, True):
@@ -273,12 +285,16 @@ def run_ours(args, world, rank, local):
     # Kb steps per B, BF16 and FP8, plus the sweep alone
     Kb = max(1, min(K, 20))
     bgraphs = {}
+    # a captured graph holds raw device pointers, not the tensors: every buffer a graph uses stays
+    # referenced here until the end of the run
+    graph_buffers = []
     for b in BATCHES:
         tokens_b, hidden_b = synth.make_step_inputs(H, V, b, 1000 + b, dev)
         tokb = torch.empty((Kb + 1, b), dtype=torch.int32, device=dev)
         tokb[0].copy_(tokens_b)
         xb = torch.empty((b, H), dtype=torch.bfloat16, device=dev)
         db = torch.empty(b, dtype=torch.int32, device=dev)
+        graph_buffers += [tokens_b, hidden_b, tokb, xb, db]
 
         def chain_b(n, fp8, tokb=tokb, hidden_b=hidden_b, xb=xb):
             Wt, s, wt = head._head(fp8)
@@ -299,6 +315,7 @@ def run_ours(args, world, rank, local):
                                                      EPS, st)
             return fn
 
+        stream.wait_stream(torch.cuda.current_stream())  # inputs were drawn on the current stream
         with torch.cuda.stream(stream):
             for fp8 in (False, True):
                 chain_b(max(W, 3), fp8)(stream)
@@ -307,8 +324,29 @@ def run_ours(args, world, rank, local):
         for fp8 in (False, True):
             bgraphs[(b, "chain", fp8)] = capture(chain_b(Kb, fp8))
             bgraphs[(b, "sweep", fp8)] = capture(sweep_b(Kb, fp8))
+    # context rows (prefill / catch-up): R rows through the input stage at once, concat kernel +
+    # tcgen05 GEMM, Kb calls per graph
+    cgraphs = {}
+    for r in CONTEXT_ROWS:
+        tokens_r, hidden_r = synth.make_step_inputs(H, V, r, 2000 + r, dev, distinct=False)
+        xr = torch.empty((r, H), dtype=torch.bfloat16, device=dev)
+        wsr = m.context_workspace(r, H, dev)
+        graph_buffers += [tokens_r, hidden_r, xr, wsr]
+
+        def ctx_fn(n, tokens_r=tokens_r, hidden_r=hidden_r, xr=xr, wsr=wsr):
+            def fn(st):
+                for _ in range(n):
+                    m.mtp_head_context_rows(head.embed, head.enorm_w, head.hnorm_w, head.eh_proj, tokens_r,
+                                            hidden_r, xr, wsr, status, EPS, st)
+            return fn
+
+        stream.wait_stream(torch.cuda.current_stream())  # inputs were drawn on the current stream
+        with torch.cuda.stream(stream):
+            ctx_fn(max(W, 3))(stream)
+        torch.cuda.synchronize()
+        cgraphs[r] = capture(ctx_fn(Kb))
     torch.cuda.synchronize()
-    for g in bgraphs.values():
+    for g in list(bgraphs.values()) + list(cgraphs.values()):
         g.replay()
     torch.cuda.synchronize()
 
@@ -325,6 +363,11 @@ def run_ours(args, world, rank, local):
             results[key] = timed_graph(g, torch.cuda.current_stream())
             barrier(world)
             launches_all += 2 * Kb if key[1] == "chain" else Kb
+        for r, g in cgraphs.items():
+            barrier(world)
+            results[("context", r)] = timed_graph(g, torch.cuda.current_stream())
+            barrier(world)
+            launches_all += 2 * Kb
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}: {m.strerror(int(status.item()))}")
     drafts = tok[1:K + 1].view(-1)
@@ -378,6 +421,14 @@ def run_ours(args, world, rank, local):
             e[f"sweep_{tag}_frac"] = round(sw["gbs"] / world / peak, 4)
         e["input_us_approx"] = round(e["head_bf16_us"] - e["sweep_bf16_us"], 2)
         batched[f"B={b}"] = e
+    tc_peak, tc_src = peak_bf16()
+    context = {}
+    for r in CONTEXT_ROWS:
+        us = max_over_ranks(results[("context", r)] / Kb, world) * 1e3
+        flops = 2.0 * r * H * 2 * H
+        context[f"R={r}"] = {"us": round(us, 2), "rows_per_s": round(r * world / (us * 1e-6), 1),
+                             "tflops": round(flops / (us * 1e-6) / 1e12, 1),
+                             "frac": round(flops / (us * 1e-6) / 1e12 / tc_peak, 4)}
     kname = "sweep_regx_kernel<BF16,H=6144,B=1>"
     achieved = sweep_bytes(2) / (results[("sweep", False)] / K * 1e-3) / 1e9
     line = {
@@ -415,6 +466,10 @@ def run_ours(args, world, rank, local):
                 "api": "mtp_head_forward_host (pinned host buffers, synchronous per step)"},
         "batched": dict(batched, steps=Kb, kernels="tensor-core input stage and sweep (mma.sync)",
                         timing="Kb-step chains / sweep loops in one CUDA graph each; frac of the measured peak"),
+        "context": dict(context, steps=Kb, peak_tflops=tc_peak, peak_source=tc_src,
+                        kernels="row-parallel concat + tcgen05 GEMM x = concat . eh_proj^T (FP32 accumulator)",
+                        timing="Kb calls in one CUDA graph; TFLOP/s of the GEMM (2 R H 2H) over the time of both "
+                               "kernels; frac of the measured bf16 burst peak"),
         "gpu_launches": 2 * K,  # the BF16 chain region `value` is timed on: 2 kernels per step
         "gpu_launches_all_timed_regions": launches_all,
         "clocks": clocks.summary(),

@@ -247,11 +247,9 @@ int mtp_head_context_rows(const uint16_t* embed, const uint16_t* enorm_w, const 
   a.hidden = target_hidden;
   a.x = x_out;
   a.status = status;
-  a.concat = static_cast<uint16_t*>(workspace);
-  a.valid = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
-                                       (static_cast<size_t>(R) * 2 * H * 2 + 255) / 256 * 256);
   a.R = R;
   a.H = H;
+  mtp::bind_context_workspace(&a, workspace);
   a.V = V;
   a.eps = eps;
   a.inv_h = 1.0 / static_cast<double>(H);

@@ -101,14 +101,18 @@ struct ContextArgs {
   int32_t* status;
   uint16_t* concat;  // workspace: [R, 2H] BF16
   int32_t* valid;    // workspace: [R] token-in-range flags
+  float* partial;    // workspace: FP32 partial sums of tiles shared between CTAs
   int R, H, V;
   float eps;
   double inv_h;
 };
 
-// Context rows (R >= 1, H a multiple of 32): concat kernel + tensor-core GEMM.
+// Context rows (R >= 1, H a multiple of 32): concat kernel + tensor-core GEMM (+ the in-order sum
+// of the partials of tiles whose k range was shared between CTAs).
 cudaError_t launch_context_rows(const ContextArgs& a, cudaStream_t stream);
+// Workspace of the context-row stage: bytes needed, and pointing a's workspace fields into ws.
 size_t context_workspace_bytes(int R, int H);
+void bind_context_workspace(ContextArgs* a, void* ws);
 
 cudaError_t launch_input_stage(const InputArgs& a, cudaStream_t stream);
 // Batched (2 <= B <= 16) input stage on tensor cores; *launched stays false when the shape is

@@ -23,10 +23,13 @@ EPS = synth.EPS
 
 def context_band(K: int) -> float:
     """Relative band (times sum_k |p_k|) of an FP32 accumulation of K exact BF16 products on the
-    tensor cores: the MMAs add K / 16 groups of 16 exact products into the FP32 accumulator, and
+    tensor cores: the MMAs add K / 16 groups of 16 exact products into FP32 accumulators, and
     each of those additions (with whatever internal alignment the hardware uses inside a group)
-    is taken to err by at most 2^-22 of the sum of |products| accumulated so far."""
-    return (K / 16 + 2) * 2.0 ** -22
+    is taken to err by at most 2^-22 of the sum of |products| accumulated so far. When the
+    product is split along k, the at most 15 FP32 additions of the split partial sums (round to
+    nearest, each within 2^-24 of a value bounded by the sum of |products|) fit in the extra
+    16 * 2^-22."""
+    return (K / 16 + 16) * 2.0 ** -22
 
 
 class Ctx:
@@ -87,12 +90,14 @@ def check_rows(c, x_gpu, ws, rows=None):
 
 
 @pytest.mark.parametrize("H,R", [
-    (256, 17),     # one row tile, one column tile, 8 k-blocks
-    (256, 300),    # three row tiles, ragged last one
-    (1024, 130),   # four column tiles, two row tiles (the second holds 2 rows)
+    (256, 17),     # one 128-row tile, 8 k-blocks split 8 ways
+    (256, 300),    # three 128-row tiles, the last with 44 rows, split 4 ways
+    (1024, 130),   # four column tiles, one 256-row tile (both accumulators, the second with 2
+                   # rows), 32 k-blocks split 11 ways (uneven ranges)
     (288, 200),    # H not a multiple of the 256-column tile: ragged last column tile
-    (96, 40),      # H below one column tile, 3 k-blocks (fewer than the ring's stages)
-    (2048, 257),
+    (96, 40),      # H below one column tile, 3 k-blocks (fewer than the ring's stages), whole tile
+    (2048, 257),   # 24 tiles (the last row tile holds one row), 64 k-blocks split 5 ways
+    (6144, 40),    # GLM hidden size, a catch-up-sized batch of rows: 24 tiles split 4 ways
 ])
 def test_context_rows_match_oracle(H, R):
     c = Ctx(H, R, seed=H + R)
@@ -101,17 +106,29 @@ def test_context_rows_match_oracle(H, R):
     check_rows(c, x, ws)
 
 
-def test_context_rows_glm_size_sampled():
-    """GLM hidden size, 512 context rows (the launch the benchmark times); oracle on sampled rows
-    at both ends of each row tile."""
-    c = Ctx(6144, 512, seed=11)
+@pytest.mark.parametrize("R", [
+    512,    # the launch the benchmark times: 48 tiles of 256 rows, each split 3 ways along k
+    1300,   # 256-row tiles, whole; the last row tile holds 20 rows (one accumulator)
+    2048,   # a whole wave of 152 tiles, then 40 tiles split along k
+    3000,   # whole tiles only (288 tiles), ragged last row tile; some tokens out of range
+])
+def test_context_rows_glm_size_sampled(R):
+    """GLM hidden size; oracle on sampled rows at both ends of row tiles and halves."""
+    c = Ctx(6144, R, seed=11 + R)
+    bad = [r for r in (5, 2999) if r < R and R == 3000]
+    if bad:
+        t = c.tokens.clone()
+        t[bad] = -3
+        c.tokens = t
     x, st, ws = c.run()
-    assert st == 0
-    check_rows(c, x, ws, rows=[0, 1, 127, 128, 300, 383, 384, 511])
+    assert st == (m.ERR_TOKEN_RANGE if bad else 0)
+    rows = sorted({0, 1, 127, 128, 255, 256, R // 2, R - 2, R - 1} | set(bad))
+    check_rows(c, x, ws, rows=rows)
 
 
-def test_context_rows_out_of_range_tokens():
-    H, R, V = 512, 150, 1000
+@pytest.mark.parametrize("H,R", [(512, 150), (2048, 150)])
+def test_context_rows_out_of_range_tokens(H, R):
+    V = 1000
     c = Ctx(H, R, V=V, seed=3)
     t = c.tokens.clone()
     t[[0, 77, 128, 149]] = torch.tensor([-1, V, 2 ** 31 - 1, -(2 ** 31)], dtype=torch.int32)
