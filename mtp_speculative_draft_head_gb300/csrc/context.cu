@@ -4,9 +4,10 @@
 // rows run at once).
 //
 // Kernels:
-//  1. context_concat_kernel: one CTA per row forms the normalised concat [enorm(e_r) | hnorm(h_r)]
-//     (the same correctly rounded BF16 values as the single-sequence kernels) into the workspace,
-//     plus a flag per row for the token check.
+//  1. context_concat_rows_kernel (few rows: one CTA per row) or context_concat_warps_kernel
+//     (many rows: one warp per vector) forms the concat rows [enorm(e_r) | hnorm(h_r)] (the same
+//     correctly rounded BF16 values as the single-sequence kernels) in the workspace, plus a
+//     flag per row for the token check.
 //  2. context_gemm_kernel: x = concat . eh_proj^T, an R x H x 2H GEMM -- compute-bound once R
 //     reaches a few hundred rows, so it runs on the fifth-generation tensor cores: 256 x 256
 //     output tiles (two 128 x 256 FP32 accumulators in TMEM sharing each eh_proj tile), operands
@@ -35,10 +36,20 @@ namespace mtp {
 
 namespace {
 
+// ------------------------------------------------------------------------------- concat
+// Both forms compute what the single-sequence kernels compute: squares of BF16 values (exact in
+// fp32) summed as double-floats, 1/rms = rsqrt(mean + eps) in fp64 split into two fp32 parts,
+// and x * w * (1/rms) rounded once to BF16 from a double-float (bf16x8_scaled_rne), so every
+// output is the correctly rounded BF16 value whatever the summation order.
+//
+// Few rows (latency-bound): one CTA of 512 threads per row, both vectors at once, a handful of
+// 16-byte pieces per thread (the shared norm prologue).
+#ifndef MTP_CTX_CAT
+#define MTP_CTX_CAT 0  // concat kernel: 0 chosen by row count, 1 one CTA per row, 2 one warp per vector
+#endif
 constexpr int kCtxNormThreads = 512;
 
-// ------------------------------------------------------------------------------- concat
-__global__ void __launch_bounds__(kCtxNormThreads) context_concat_kernel(const ContextArgs a) {
+__global__ void __launch_bounds__(kCtxNormThreads) context_concat_rows_kernel(const ContextArgs a) {
   __shared__ float red[2 * (2 * kCtxNormThreads / 32 + 2)];
   __shared__ int ok_s;
   const int r = blockIdx.x;
@@ -62,6 +73,97 @@ __global__ void __launch_bounds__(kCtxNormThreads) context_concat_kernel(const C
     return NormJob{a.hidden + static_cast<size_t>(r) * H, a.hnorm_w, c + H, true};
   };
   rms_norm_multi_to_smem<kCtxNormThreads>(2, H, a.inv_h, a.eps, red, job, LayoutIdentity{});
+  pdl_launch_dependents();
+}
+
+// Many rows (bandwidth-bound): one warp per normalised vector (vector 2r: enorm of the embedding
+// row of tokens[r]; 2r + 1: hnorm of hidden row r), no block-level synchronisation, many vectors
+// in flight per SM. Pass 1 reads x in batches of kCatBatch 16-byte pieces per lane (all in
+// flight together) into four independent double-float sums; pass 2 reads x again (L1 / L2) with
+// the norm weight, again a batch at a time.
+constexpr int kCatWarps = 8;
+constexpr int kCatBatch = 8;
+
+__global__ void __launch_bounds__(kCatWarps * 32, 4) context_concat_warps_kernel(const ContextArgs a) {
+  pdl_wait_prior_grid();  // tokens and target_hidden may come from the preceding kernel
+  const int lane = threadIdx.x & 31;
+  const int H = a.H, nv8 = a.H / 8;
+  const int64_t nvec = 2 * static_cast<int64_t>(a.R);
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t vec = static_cast<int64_t>(blockIdx.x) * kCatWarps + (threadIdx.x >> 5); vec < nvec;
+       vec += static_cast<int64_t>(gridDim.x) * kCatWarps) {
+    const int r = static_cast<int>(vec >> 1), half = static_cast<int>(vec & 1);
+    const uint16_t* x;
+    const uint16_t* w;
+    bool ok = true;
+    if (half == 0) {
+      const int32_t tok = a.tokens[r];
+      ok = tok >= 0 && tok < a.V;
+      if (lane == 0) {
+        a.valid[r] = ok ? 1 : 0;
+        if (!ok) store_status(a.status, MTP_ERR_TOKEN_RANGE);
+      }
+      x = a.embed + static_cast<int64_t>(ok ? tok : 0) * H;
+      w = a.enorm_w;
+    } else {
+      x = a.hidden + static_cast<size_t>(r) * H;
+      w = a.hnorm_w;
+    }
+    uint4* out = reinterpret_cast<uint4*>(a.concat + static_cast<size_t>(r) * 2 * H + static_cast<size_t>(half) * H);
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    const uint4* wv = reinterpret_cast<const uint4*>(w);
+    if (!ok) {  // the embedding table is not read for an out-of-range token
+      for (int v = lane; v < nv8; v += 32) out[v] = z;
+      continue;
+    }
+    DF acc[4] = {DF{0.0f, 0.0f}, DF{0.0f, 0.0f}, DF{0.0f, 0.0f}, DF{0.0f, 0.0f}};
+    for (int v0 = 0; v0 < nv8; v0 += 32 * kCatBatch) {
+      uint4 q[kCatBatch];
+#pragma unroll
+      for (int i = 0; i < kCatBatch; ++i) {
+        const int v = v0 + 32 * i + lane;
+        q[i] = v < nv8 ? xv[v] : z;
+      }
+#pragma unroll
+      for (int i = 0; i < kCatBatch; ++i) {
+        const uint32_t u[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float lo = bf16_lo(u[t]), hi = bf16_hi(u[t]);
+          df_add(acc[t], __fmul_rn(lo, lo));
+          df_add(acc[t], __fmul_rn(hi, hi));
+        }
+      }
+    }
+    DF tot = df_add(df_add(acc[0], acc[1]), df_add(acc[2], acc[3]));
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) tot = df_add(tot, shfl_xor_df(tot, m));
+    const double ms = (static_cast<double>(tot.hi) + static_cast<double>(tot.lo)) * a.inv_h;
+    const double rinv = rsqrt(ms + static_cast<double>(a.eps));
+    const float rh = static_cast<float>(rinv);
+    const float rl = static_cast<float>(rinv - static_cast<double>(rh));
+    constexpr int kB2 = kCatBatch / 2;
+    for (int v0 = 0; v0 < nv8; v0 += 32 * kB2) {
+      uint4 xq[kB2], wq[kB2];
+#pragma unroll
+      for (int i = 0; i < kB2; ++i) {
+        const int v = v0 + 32 * i + lane;
+        xq[i] = v < nv8 ? xv[v] : z;
+        wq[i] = v < nv8 ? wv[v] : z;
+      }
+#pragma unroll
+      for (int i = 0; i < kB2; ++i) {
+        const int v = v0 + 32 * i + lane;
+        if (v < nv8) {
+          const uint32_t xu[4] = {xq[i].x, xq[i].y, xq[i].z, xq[i].w};
+          const uint4 w4 = wq[i];
+          const float wf[8] = {bf16_lo(w4.x), bf16_hi(w4.x), bf16_lo(w4.y), bf16_hi(w4.y),
+                               bf16_lo(w4.z), bf16_hi(w4.z), bf16_lo(w4.w), bf16_hi(w4.w)};
+          out[v] = bf16x8_scaled_rne(xu, wf, rh, rl);
+        }
+      }
+    }
+  }
   pdl_launch_dependents();
 }
 
@@ -425,8 +527,17 @@ cudaError_t launch_context_rows(const ContextArgs& in, cudaStream_t stream) {
   }
   {
     void* params[] = {&a};
-    err = launch_pdl(reinterpret_cast<const void*>(context_concat_kernel), dim3(static_cast<unsigned>(a.R)),
-                     dim3(kCtxNormThreads), 0, stream, params);
+    // one warp per vector once there are enough vectors (measured: from about a thousand rows)
+    const bool warps = MTP_CTX_CAT == 2 || (MTP_CTX_CAT == 0 && 2 * static_cast<int64_t>(a.R) >= 2LL * kCatWarps * di.sm_count);
+    if (warps) {
+      int64_t blocks = (2 * static_cast<int64_t>(a.R) + kCatWarps - 1) / kCatWarps;
+      if (blocks > 4 * di.sm_count) blocks = 4 * di.sm_count;
+      err = launch_pdl(reinterpret_cast<const void*>(context_concat_warps_kernel),
+                       dim3(static_cast<unsigned>(blocks)), dim3(kCatWarps * 32), 0, stream, params);
+    } else {
+      err = launch_pdl(reinterpret_cast<const void*>(context_concat_rows_kernel), dim3(static_cast<unsigned>(a.R)),
+                       dim3(kCtxNormThreads), 0, stream, params);
+    }
     if (err != cudaSuccess) return err;
   }
   {
