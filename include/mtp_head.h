@@ -108,7 +108,8 @@ int mtp_head_input(const uint16_t* embed, const uint16_t* enorm_w, const uint16_
  *   x_out          [R, H]  BF16   output; a row whose token is outside [0, V) is zeros and
  *                                 status (optional) gets MTP_ERR_TOKEN_RANGE
  *   workspace             device scratch of at least mtp_head_context_workspace_bytes(R, H)
- *                         bytes (no initialisation needed; may be NULL when R <= 16)
+ *                         bytes (no initialisation needed; may be NULL when R <= 16, in which
+ *                         case the batched input stage normalises the rows in every CTA)
  *   R              1 .. 65536 rows
  *
  * R <= 16 runs the batched input stage (one pass over eh_proj for all rows). Larger R runs two
@@ -181,7 +182,14 @@ int mtp_head_logits_argmax_batched_noalloc(const uint16_t* x, const uint16_t* fi
                                            int32_t* status, int B, int H, int V, float eps,
                                            void* stream);
 
-/* Bytes of workspace the output stage needs (no device query; 0 for invalid shapes). */
+/* Bytes of workspace for the output stage and the whole-step entry points (no device query; 0
+ * for invalid shapes): the output stage's part (the first 128 + 8192 * B bytes, which must be
+ * zero-filled once), then room for the batched input stage's prebuilt concat (2B * H BF16 and B
+ * row flags; no initialisation needed). The output stage alone accepts any workspace of at least
+ * its own part. mtp_head_forward_batched / _host given a workspace of the full size build the
+ * concat of B >= 6 sequences once, with one row-parallel kernel, and the tensor-core input
+ * stage copies it instead of normalising it in every CTA (the same values); otherwise the input
+ * stage builds it itself. */
 size_t mtp_head_workspace_bytes(int B, int H, int V);
 
 /* ------------------------------------------------------------------------------------------

@@ -62,10 +62,26 @@ int validate_output(const uint16_t* x, const uint16_t* final_norm_w, const void*
   return MTP_OK;
 }
 
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Workspace of the whole-step entry points: the output stage's part, then room for the prebuilt
+// concat of the batched input stage ([B, 2H] BF16, then [B] int32 row flags).
+size_t step_concat_offset(int B) { return round256(mtp::sweep_workspace_bytes(B)); }
+size_t step_workspace_bytes(int B, int H) {
+  return step_concat_offset(B) + round256(static_cast<size_t>(B) * 2 * H * 2) + round256(static_cast<size_t>(B) * 4);
+}
+
+// cat_ws (may be null): workspace for a prebuilt concat, [B, 2H] BF16 then the [B] row flags
+// 256-byte aligned after it.
 int run_input(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hnorm_w,
               const uint16_t* eh_proj, const int32_t* tokens, const uint16_t* target_hidden,
-              uint16_t* x_out, int32_t* status, int B, int H, int V, float eps, void* stream) {
+              uint16_t* x_out, int32_t* status, int B, int H, int V, float eps, void* stream,
+              void* cat_ws = nullptr) {
   mtp::InputArgs a{};
+  if (cat_ws != nullptr) {
+    a.concat_ws = static_cast<uint16_t*>(cat_ws);
+    a.valid_ws = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(cat_ws) + round256(static_cast<size_t>(B) * 2 * H * 2));
+  }
   a.embed = embed;
   a.enorm_w = enorm_w;
   a.hnorm_w = hnorm_w;
@@ -158,7 +174,7 @@ int mtp_head_logits_argmax(const uint16_t* x, const uint16_t* final_norm_w, cons
 
 size_t mtp_head_workspace_bytes(int B, int H, int V) {
   if (check_shape(B, H, V) != MTP_OK) return 0;
-  return mtp::sweep_workspace_bytes(B);
+  return step_workspace_bytes(B, H);
 }
 
 int mtp_head_forward_batched(const uint16_t* embed, const uint16_t* enorm_w,
@@ -174,8 +190,11 @@ int mtp_head_forward_batched(const uint16_t* embed, const uint16_t* enorm_w,
   v = validate_output(x, final_norm_w, lm_head, row_scale, w_dtype, logits, draft, status, workspace,
                       workspace_bytes, B, H, V, eps);
   if (v != MTP_OK) return v;
+  // a workspace of the full size also takes the prebuilt concat of the batched input stage
+  void* cat = workspace_bytes >= step_workspace_bytes(B, H) ? static_cast<uint8_t*>(workspace) + step_concat_offset(B)
+                                                             : nullptr;
   v = run_input(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidden, x, status, B, H, V, eps,
-                stream);
+                stream, cat);
   if (v != MTP_OK) return v;
   return run_output(x, final_norm_w, lm_head, row_scale, w_dtype, logits, draft, status, workspace,
                     B, H, V, eps, stream);
@@ -202,8 +221,10 @@ int mtp_head_forward_host(const uint16_t* embed, const uint16_t* enorm_w, const 
   if (cudaMemcpyAsync(hidden_dev, hidden_host, sizeof(uint16_t) * static_cast<size_t>(B) * H,
                       cudaMemcpyHostToDevice, st) != cudaSuccess)
     return MTP_ERR_CUDA;
+  void* cat = workspace_bytes >= step_workspace_bytes(B, H) ? static_cast<uint8_t*>(workspace) + step_concat_offset(B)
+                                                             : nullptr;
   v = run_input(embed, enorm_w, hnorm_w, eh_proj, tokens_dev, hidden_dev, x_dev, status, B, H, V,
-                eps, stream);
+                eps, stream, cat);
   if (v != MTP_OK) return v;
   v = run_output(x_dev, final_norm_w, lm_head, row_scale, w_dtype, nullptr, draft_dev, status,
                  workspace, B, H, V, eps, stream);
@@ -233,9 +254,12 @@ int mtp_head_context_rows(const uint16_t* embed, const uint16_t* enorm_w, const 
       !aligned(target_hidden, 16) || !aligned(x_out, 16) || !aligned(tokens, 4) ||
       (status && !aligned(status, 4)) || (workspace && !aligned(workspace, 16)))
     return MTP_ERR_ALIGN;
-  if (R <= kMaxB)  // a few rows: the batched input stage, one weight pass for all of them
+  if (R <= kMaxB) {  // a few rows: the batched input stage, one weight pass for all of them
+    // its concat and row flags sit where this entry point's own kernels put them
+    void* cat = (workspace && workspace_bytes >= mtp::context_workspace_bytes(R, H)) ? workspace : nullptr;
     return run_input(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidden, x_out, status, R, H, V, eps,
-                     stream);
+                     stream, cat);
+  }
   if (H % 32 != 0) return MTP_ERR_NOT_IMPLEMENTED;
   if (!workspace || workspace_bytes < mtp::context_workspace_bytes(R, H)) return MTP_ERR_WORKSPACE;
   mtp::ContextArgs a{};

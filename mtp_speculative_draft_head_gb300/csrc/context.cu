@@ -55,6 +55,10 @@ __global__ void __launch_bounds__(kCtxNormThreads) context_concat_rows_kernel(co
   const int r = blockIdx.x;
   const int H = a.H;
   pdl_wait_prior_grid();  // tokens and target_hidden may come from the preceding kernel
+  // The next kernel may start its independent work (weight streams) now; it waits for this
+  // grid's completion before it reads the concat. Every CTA of this grid has started by the
+  // time the next one launches, so it never holds SMs this grid still needs.
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     const int32_t tok = a.tokens[r];
     const int ok = (tok >= 0 && tok < a.V) ? 1 : 0;
@@ -73,7 +77,6 @@ __global__ void __launch_bounds__(kCtxNormThreads) context_concat_rows_kernel(co
     return NormJob{a.hidden + static_cast<size_t>(r) * H, a.hnorm_w, c + H, true};
   };
   rms_norm_multi_to_smem<kCtxNormThreads>(2, H, a.inv_h, a.eps, red, job, LayoutIdentity{});
-  pdl_launch_dependents();
 }
 
 // Many rows (bandwidth-bound): one warp per normalised vector (vector 2r: enorm of the embedding
@@ -490,6 +493,24 @@ void bind_context_workspace(ContextArgs* a, void* ws) {
   a->partial = reinterpret_cast<float*>(p);
 }
 
+cudaError_t launch_context_concat(const ContextArgs& in, cudaStream_t stream) {
+  DeviceInfo di;
+  cudaError_t err = device_info(&di);
+  if (err != cudaSuccess) return err;
+  ContextArgs a = in;
+  void* params[] = {&a};
+  // one warp per vector once there are enough vectors (measured: from about a thousand rows)
+  const bool warps = MTP_CTX_CAT == 2 || (MTP_CTX_CAT == 0 && 2 * static_cast<int64_t>(a.R) >= 2LL * kCatWarps * di.sm_count);
+  if (warps) {
+    int64_t blocks = (2 * static_cast<int64_t>(a.R) + kCatWarps - 1) / kCatWarps;
+    if (blocks > 4 * di.sm_count) blocks = 4 * di.sm_count;
+    return launch_pdl(reinterpret_cast<const void*>(context_concat_warps_kernel), dim3(static_cast<unsigned>(blocks)),
+                      dim3(kCatWarps * 32), 0, stream, params);
+  }
+  return launch_pdl(reinterpret_cast<const void*>(context_concat_rows_kernel), dim3(static_cast<unsigned>(a.R)),
+                    dim3(kCtxNormThreads), 0, stream, params);
+}
+
 cudaError_t launch_context_rows(const ContextArgs& in, cudaStream_t stream) {
   DeviceInfo di;
   cudaError_t err = device_info(&di);
@@ -525,21 +546,8 @@ cudaError_t launch_context_rows(const ContextArgs& in, cudaStream_t stream) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorNotSupported;
   }
-  {
-    void* params[] = {&a};
-    // one warp per vector once there are enough vectors (measured: from about a thousand rows)
-    const bool warps = MTP_CTX_CAT == 2 || (MTP_CTX_CAT == 0 && 2 * static_cast<int64_t>(a.R) >= 2LL * kCatWarps * di.sm_count);
-    if (warps) {
-      int64_t blocks = (2 * static_cast<int64_t>(a.R) + kCatWarps - 1) / kCatWarps;
-      if (blocks > 4 * di.sm_count) blocks = 4 * di.sm_count;
-      err = launch_pdl(reinterpret_cast<const void*>(context_concat_warps_kernel),
-                       dim3(static_cast<unsigned>(blocks)), dim3(kCatWarps * 32), 0, stream, params);
-    } else {
-      err = launch_pdl(reinterpret_cast<const void*>(context_concat_rows_kernel), dim3(static_cast<unsigned>(a.R)),
-                       dim3(kCtxNormThreads), 0, stream, params);
-    }
-    if (err != cudaSuccess) return err;
-  }
+  err = launch_context_concat(a, stream);
+  if (err != cudaSuccess) return err;
   {
     CUtensorMap tac = ta, tbc = tb;
     void* params[] = {&tac, &tbc, &a, &c};

@@ -72,6 +72,12 @@ struct InputArgs {
   double inv_h;  // 1 / H (fp64), for the mean of squares
   int stages;  // pipeline stages (bulk-copy kernel)
   int group;   // sequences whose concat is resident at once (plain kernel)
+  // Optional caller workspace for a prebuilt concat ([B, 2H] BF16, then [B] int32 row flags):
+  // when given, the tensor-core kernel's launcher builds the concat there once (the row-parallel
+  // concat kernel) and the kernel copies it instead of normalising it in every CTA.
+  uint16_t* concat_ws;
+  int32_t* valid_ws;
+  const uint16_t* concat;  // set by that launcher: the prebuilt concat the kernel reads
 };
 
 struct SweepArgs {
@@ -110,6 +116,9 @@ struct ContextArgs {
 // Context rows (R >= 1, H a multiple of 32): concat kernel + tensor-core GEMM (+ the in-order sum
 // of the partials of tiles whose k range was shared between CTAs).
 cudaError_t launch_context_rows(const ContextArgs& a, cudaStream_t stream);
+// The first kernel of that path alone: the normalised concat rows and row flags into
+// a.concat / a.valid.
+cudaError_t launch_context_concat(const ContextArgs& a, cudaStream_t stream);
 // Workspace of the context-row stage: bytes needed, and pointing a's workspace fields into ws.
 size_t context_workspace_bytes(int R, int H);
 void bind_context_workspace(ContextArgs* a, void* ws);

@@ -412,3 +412,28 @@ def test_fp8_every_code_including_subnormals(H):
     np.testing.assert_allclose(lg, ref, rtol=1e-4, atol=1e-6 * np.abs(ref).max())
     assert lg[0, 0] != 0.0 and lg[0, 1] != 0.0
     check_logits_and_draft(logits.cpu().numpy(), draft.cpu().numpy(), ref, TOL_FP8)
+
+
+@pytest.mark.parametrize("H,B", [(6144, 16), (1024, 6), (2048, 8), (96, 9), (1024, 2)])
+def test_prebuilt_concat_gives_the_same_x(H, B):
+    """With a full-size workspace and B >= 6 the whole-step entry point builds the batch's concat
+    once (row kernel) and the tensor-core input stage copies it; without one,
+    mtp_head_input_batched normalises in every CTA (as the whole step does for B < 6). Same
+    arithmetic, so x must be identical bit for bit -- including the zero row of an out-of-range
+    token -- and the status the same."""
+    c = Case(H, 700, B, seed=H + 3 * B)
+    tokens = c.tokens.clone()
+    tokens[B // 2] = c.V + 5
+    x_in, st_in = c.input_gpu(tokens=tokens)
+    assert st_in == m.ERR_TOKEN_RANGE
+    assert c.ws.numel() >= m.mtp_head_workspace_bytes(B, H, c.V)
+    x_fw = torch.full((B, H), 7, dtype=torch.bfloat16, device=DEV)
+    d = torch.empty(B, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.mtp_head_forward_batched(c.g["embed"], c.g["enorm_w"], c.g["hnorm_w"], c.g["eh_proj"], c.g["final_norm_w"],
+                               c.g["lm_head"], None, m.W_BF16, tokens.to(DEV), c.hidden.to(DEV), x_fw, None, d,
+                               c.ws, st, EPS)
+    torch.cuda.synchronize()
+    assert int(st.item()) == m.ERR_TOKEN_RANGE
+    assert torch.equal(x_fw.view(torch.int16), x_in.view(torch.int16))
+    assert bool((x_fw[B // 2].view(torch.int16) == 0).all())
