@@ -381,23 +381,22 @@ def run_ours(args, world, rank, local):
     inp = aggregate(results[("input", None)], input_bytes(), K, world)
 
     # end to end through the host-buffer entry point: inputs copied in and the draft copied out
-    # every step, synchronous like the source's forward_one
+    # every step, synchronous like the source's forward_one (a prepared HostStep: the device
+    # buffers are bound once, each call passes the three pinned host buffers)
     ke = min(K, 200)
     hid_host = hiddens[:n_hidden].cpu().pin_memory()
     th = torch.empty(1, dtype=torch.int32).pin_memory()
     dh = torch.empty(1, dtype=torch.int32).pin_memory()
-    td = torch.empty(1, dtype=torch.int32, device=dev)
-    hd = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
-    xd = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
-    dd = torch.empty(1, dtype=torch.int32, device=dev)
+    step = head.host_step(1, fp8=False, stream=stream)
+    th_np, dh_np = th.numpy(), dh.numpy()
+    th_p, dh_p = th.data_ptr(), dh.data_ptr()
+    hid_p = [hid_host[i].data_ptr() for i in range(n_hidden)]
 
     def e2e_steps(n):
-        th[0] = int(first.item())
+        th_np[0] = int(first.item())
         for i in range(n):
-            m.mtp_head_forward_host(head.embed, head.enorm_w, head.hnorm_w, head.eh_proj, head.final_norm_w,
-                                    head.lm_head, None, m.W_BF16, th, hid_host[i % n_hidden], td, hd, xd, dd,
-                                    dh, head.ws, None, EPS, stream)
-            th[0] = dh[0]
+            step(th_p, hid_p[i % n_hidden], dh_p)
+            th_np[0] = dh_np[0]
 
     e2e_steps(W)
     torch.cuda.synchronize()
@@ -463,7 +462,7 @@ def run_ours(args, world, rank, local):
                      "timing": "K back-to-back launches in one CUDA graph, CUDA events on the launching stream"},
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "us_per_step": round(e2e_ms / ke * 1e3, 2),
                 "h2d_bytes_per_step": 4 + H * 2, "d2h_bytes_per_step": 4, "steps": ke,
-                "api": "mtp_head_forward_host (pinned host buffers, synchronous per step)"},
+                "api": "mtp_head_forward_host through HostStep (pinned host buffers, synchronous per step)"},
         "batched": dict(batched, steps=Kb, kernels="tensor-core input stage and sweep (mma.sync)",
                         timing="Kb-step chains / sweep loops in one CUDA graph each; frac of the measured peak"),
         "context": dict(context, steps=Kb, peak_tflops=tc_peak, peak_source=tc_src,

@@ -212,6 +212,15 @@ int mtp_head_forward_batched(const uint16_t* embed, const uint16_t* enorm_w,
  * tokens_dev / hidden_dev, runs mtp_head_forward_batched, copies draft back into
  * draft_host [B] and waits for the stream. Host buffers should be pinned for asynchronous
  * copies. The device `status` word, if given, is read back too and returned when nonzero.
+ *
+ * On a stream other than the legacy default stream (and not under the caller's own capture),
+ * the first call for a given set of device buffers, shapes, eps and stream runs operation by
+ * operation and then records the step in a CUDA graph around small pinned staging buffers
+ * (held by the library, at most 8 such steps, least recently used replaced). Later calls with
+ * the same set copy the host inputs into the staging buffers, launch the graph once, wait, and
+ * copy the draft out: the same work, without a launch per operation. The host buffers may
+ * differ from call to call. Calls from several threads are safe; calls sharing a recorded
+ * step are serialised.
  * ---------------------------------------------------------------------------------------- */
 int mtp_head_forward_host(const uint16_t* embed, const uint16_t* enorm_w,
                           const uint16_t* hnorm_w, const uint16_t* eh_proj,

@@ -8,7 +8,7 @@ buffers around them. PyTorch provides device memory and streams only.
 """
 from ._lib import (  # noqa: F401
     ERR_ALIGN, ERR_ARG, ERR_CUDA, ERR_NONFINITE, ERR_NOT_IMPLEMENTED, ERR_SHAPE, ERR_TIMEOUT,
-    ERR_TOKEN_RANGE, ERR_WORKSPACE, OK, W_BF16, W_FP8_E4M3, MTPError, SIGNATURES, context_workspace, load,
+    ERR_TOKEN_RANGE, ERR_WORKSPACE, OK, W_BF16, W_FP8_E4M3, HostStep, MTPError, SIGNATURES, context_workspace, load,
     mtp_head_context_rows, mtp_head_context_workspace_bytes,
     mtp_head_forward_batched, mtp_head_forward_host, mtp_head_input, mtp_head_input_batched,
     mtp_head_logits_argmax, mtp_head_logits_argmax_batched,

@@ -238,6 +238,36 @@ def mtp_head_forward_host(embed, enorm_w, hnorm_w, eh_proj, final_norm_w, lm_hea
         "mtp_head_forward_host")
 
 
+class HostStep:
+    """mtp_head_forward_host with its device buffers bound once: a call passes only the three host
+    buffers (tensors, or their addresses as ints), so a synchronous draft step costs one ctypes
+    call on the host. The bound tensors stay referenced for the object's lifetime."""
+
+    def __init__(self, embed, enorm_w, hnorm_w, eh_proj, final_norm_w, lm_head, row_scale, w_dtype: int,
+                 tokens_dev, hidden_dev, x_dev, draft_dev, ws, status=None, eps: float = 1e-6, stream=None):
+        V, H = embed.shape
+        B = tokens_dev.numel()
+        self.B, self.H, self.V = B, H, V
+        self._keep = (embed, enorm_w, hnorm_w, eh_proj, final_norm_w, lm_head, row_scale, tokens_dev,
+                      hidden_dev, x_dev, draft_dev, ws, status, stream)
+        self._fn = load().mtp_head_forward_host
+        self._head = (_dev(embed, "embed"), _dev(enorm_w, "enorm_w"), _dev(hnorm_w, "hnorm_w"),
+                      _dev(eh_proj, "eh_proj"), _dev(final_norm_w, "final_norm_w"), _dev(lm_head, "lm_head"),
+                      _dev(row_scale, "row_scale"), int(w_dtype))
+        self._mid = (_dev(tokens_dev, "tokens_dev"), _dev(hidden_dev, "hidden_dev"), _dev(x_dev, "x_dev"),
+                     _dev(draft_dev, "draft_dev"))
+        self._tail = (_dev(status, "status"), _dev(ws, "workspace"), ws.numel() * ws.element_size(), B, H, V,
+                      float(eps), _stream(stream))
+
+    def __call__(self, tokens_host, hidden_host, draft_host) -> None:
+        t = tokens_host if isinstance(tokens_host, int) else tokens_host.data_ptr()
+        h = hidden_host if isinstance(hidden_host, int) else hidden_host.data_ptr()
+        d = draft_host if isinstance(draft_host, int) else draft_host.data_ptr()
+        code = self._fn(*self._head, t, h, *self._mid, d, *self._tail)
+        if code != OK:
+            raise MTPError(code, "mtp_head_forward_host")
+
+
 def mtp_head_quantize_fp8(w, q, row_scale, status, stream=None) -> None:
     V, H = w.shape
     _check(load().mtp_head_quantize_fp8(

@@ -4,6 +4,11 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
+
+#include <memory>
+#include <mutex>
+#include <vector>
 
 #include "../../include/mtp_head.h"
 #include "common.cuh"
@@ -119,6 +124,175 @@ int run_output(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_h
   return map_cuda(mtp::launch_sweep(a, static_cast<cudaStream_t>(stream)));
 }
 
+// ------------------------------------------------------------------------------------------
+// The host-buffer whole step. Each call copies the inputs in, runs both stages, copies the draft
+// out and waits, like the source's forward_one. Launching those five or six operations one by
+// one costs several microseconds of host time each, and the GPU idles meanwhile, so the first
+// call for a given set of device buffers, shapes and stream runs directly and then records the
+// step in a CUDA graph around small pinned staging buffers; later calls copy the host inputs into
+// the staging buffers (a few KB), launch the graph once, wait, and copy the draft out. A stream
+// that is the legacy default stream, or is being captured by the caller, always runs directly.
+struct HostStep {
+  const uint16_t* embed;
+  const uint16_t* enorm_w;
+  const uint16_t* hnorm_w;
+  const uint16_t* eh_proj;
+  const uint16_t* final_norm_w;
+  const void* lm_head;
+  const float* row_scale;
+  int w_dtype;
+  int32_t* tokens_dev;
+  uint16_t* hidden_dev;
+  uint16_t* x_dev;
+  int32_t* draft_dev;
+  int32_t* status;
+  void* workspace;
+  size_t workspace_bytes;
+  int B, H, V;
+  float eps;
+  cudaStream_t stream;
+
+  bool same(const HostStep& o) const {
+    return embed == o.embed && enorm_w == o.enorm_w && hnorm_w == o.hnorm_w && eh_proj == o.eh_proj &&
+           final_norm_w == o.final_norm_w && lm_head == o.lm_head && row_scale == o.row_scale &&
+           w_dtype == o.w_dtype && tokens_dev == o.tokens_dev && hidden_dev == o.hidden_dev && x_dev == o.x_dev &&
+           draft_dev == o.draft_dev && status == o.status && workspace == o.workspace &&
+           workspace_bytes == o.workspace_bytes && B == o.B && H == o.H && V == o.V &&
+           memcmp(&eps, &o.eps, sizeof(float)) == 0 && stream == o.stream;
+  }
+};
+
+// Queue one step on s.stream: inputs from tok/hid (host), draft to draft_out, the status word
+// to status_out when both it and s.status are given.
+int enqueue_host_step(const HostStep& s, const int32_t* tok, const uint16_t* hid, int32_t* draft_out,
+                      int32_t* status_out) {
+  const size_t hid_bytes = sizeof(uint16_t) * static_cast<size_t>(s.B) * s.H;
+  if (cudaMemcpyAsync(s.tokens_dev, tok, sizeof(int32_t) * s.B, cudaMemcpyHostToDevice, s.stream) != cudaSuccess)
+    return MTP_ERR_CUDA;
+  if (cudaMemcpyAsync(s.hidden_dev, hid, hid_bytes, cudaMemcpyHostToDevice, s.stream) != cudaSuccess)
+    return MTP_ERR_CUDA;
+  void* cat = s.workspace_bytes >= step_workspace_bytes(s.B, s.H)
+                  ? static_cast<uint8_t*>(s.workspace) + step_concat_offset(s.B)
+                  : nullptr;
+  int v = run_input(s.embed, s.enorm_w, s.hnorm_w, s.eh_proj, s.tokens_dev, s.hidden_dev, s.x_dev, s.status, s.B,
+                    s.H, s.V, s.eps, s.stream, cat);
+  if (v != MTP_OK) return v;
+  v = run_output(s.x_dev, s.final_norm_w, s.lm_head, s.row_scale, s.w_dtype, nullptr, s.draft_dev, s.status,
+                 s.workspace, s.B, s.H, s.V, s.eps, s.stream);
+  if (v != MTP_OK) return v;
+  if (cudaMemcpyAsync(draft_out, s.draft_dev, sizeof(int32_t) * s.B, cudaMemcpyDeviceToHost, s.stream) != cudaSuccess)
+    return MTP_ERR_CUDA;
+  if (s.status && status_out &&
+      cudaMemcpyAsync(status_out, s.status, sizeof(int32_t), cudaMemcpyDeviceToHost, s.stream) != cudaSuccess)
+    return MTP_ERR_CUDA;
+  return MTP_OK;
+}
+
+struct StepGraph {
+  HostStep key;
+  int device = -1;
+  std::mutex mu;  // one call at a time uses the staging buffers
+  cudaGraphExec_t exec = nullptr;
+  int32_t* tok = nullptr;     // pinned staging: [B] tokens, [B, H] hidden, [B] draft, status
+  uint16_t* hid = nullptr;
+  int32_t* draft = nullptr;
+  int32_t* st = nullptr;
+  uint64_t last_use = 0;
+  ~StepGraph() {
+    if (exec) cudaGraphExecDestroy(exec);
+    if (tok) cudaFreeHost(tok);
+  }
+};
+
+constexpr size_t kMaxStepGraphs = 8;
+std::mutex g_step_mu;
+// never destroyed: at process exit the CUDA runtime may already be gone
+std::vector<std::shared_ptr<StepGraph>>* g_steps = new std::vector<std::shared_ptr<StepGraph>>();
+uint64_t g_step_clock = 0;
+
+// Records the step into a new graph around freshly allocated staging buffers; null on failure
+// (the caller then keeps running directly).
+std::shared_ptr<StepGraph> record_step(const HostStep& s, int device) {
+  auto g = std::make_shared<StepGraph>();
+  g->key = s;
+  g->device = device;
+  const size_t hid_bytes = sizeof(uint16_t) * static_cast<size_t>(s.B) * s.H;
+  const size_t tok_bytes = (sizeof(int32_t) * s.B + 15) / 16 * 16;
+  uint8_t* base = nullptr;
+  if (cudaHostAlloc(reinterpret_cast<void**>(&base), 2 * tok_bytes + 16 + hid_bytes, cudaHostAllocDefault) !=
+      cudaSuccess)
+    return nullptr;
+  g->tok = reinterpret_cast<int32_t*>(base);
+  g->draft = reinterpret_cast<int32_t*>(base + tok_bytes);
+  g->st = reinterpret_cast<int32_t*>(base + 2 * tok_bytes);
+  g->hid = reinterpret_cast<uint16_t*>(base + 2 * tok_bytes + 16);
+  if (cudaStreamBeginCapture(s.stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return nullptr;
+  const int v = enqueue_host_step(s, g->tok, g->hid, g->draft, g->st);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(s.stream, &graph);
+  if (v != MTP_OK || e != cudaSuccess || graph == nullptr) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();
+    return nullptr;
+  }
+  const cudaError_t ei = cudaGraphInstantiate(&g->exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ei != cudaSuccess) {
+    g->exec = nullptr;
+    cudaGetLastError();
+    return nullptr;
+  }
+  return g;
+}
+
+int run_host_step(const HostStep& s, const int32_t* tokens_host, const uint16_t* hidden_host, int32_t* draft_host) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return MTP_ERR_CUDA;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const bool can_graph = s.stream != nullptr && cudaStreamIsCapturing(s.stream, &cs) == cudaSuccess &&
+                         cs == cudaStreamCaptureStatusNone;
+  std::shared_ptr<StepGraph> g;
+  bool first = false;
+  if (can_graph) {
+    std::lock_guard<std::mutex> lock(g_step_mu);
+    for (auto& e : *g_steps)
+      if (e->device == device && e->key.same(s)) g = e;
+    first = g == nullptr;
+    if (g) g->last_use = ++g_step_clock;
+  }
+  if (!g) {
+    // directly: the caller's host buffers, operation by operation
+    int32_t dev_status = 0;
+    int v = enqueue_host_step(s, tokens_host, hidden_host, draft_host, &dev_status);
+    if (v != MTP_OK) return v;
+    if (cudaStreamSynchronize(s.stream) != cudaSuccess) return MTP_ERR_CUDA;
+    if (first) {  // everything is initialised now: record the step for the next calls
+      std::shared_ptr<StepGraph> rec = record_step(s, device);
+      if (rec) {
+        std::lock_guard<std::mutex> lock(g_step_mu);
+        rec->last_use = ++g_step_clock;
+        if (g_steps->size() >= kMaxStepGraphs) {
+          size_t lru = 0;
+          for (size_t i = 1; i < g_steps->size(); ++i)
+            if ((*g_steps)[i]->last_use < (*g_steps)[lru]->last_use) lru = i;
+          (*g_steps)[lru] = rec;
+        } else {
+          g_steps->push_back(rec);
+        }
+      }
+    }
+    return s.status ? dev_status : MTP_OK;
+  }
+  std::lock_guard<std::mutex> lock(g->mu);
+  memcpy(g->tok, tokens_host, sizeof(int32_t) * s.B);
+  memcpy(g->hid, hidden_host, sizeof(uint16_t) * static_cast<size_t>(s.B) * s.H);
+  *g->st = 0;
+  if (cudaGraphLaunch(g->exec, s.stream) != cudaSuccess) return MTP_ERR_CUDA;
+  if (cudaStreamSynchronize(s.stream) != cudaSuccess) return MTP_ERR_CUDA;
+  memcpy(draft_host, g->draft, sizeof(int32_t) * s.B);
+  return s.status ? *g->st : MTP_OK;
+}
+
 }  // namespace
 
 namespace mtp {
@@ -215,27 +389,9 @@ int mtp_head_forward_host(const uint16_t* embed, const uint16_t* enorm_w, const 
   v = validate_output(x_dev, final_norm_w, lm_head, row_scale, w_dtype, nullptr, draft_dev, status,
                       workspace, workspace_bytes, B, H, V, eps);
   if (v != MTP_OK) return v;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(tokens_dev, tokens_host, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return MTP_ERR_CUDA;
-  if (cudaMemcpyAsync(hidden_dev, hidden_host, sizeof(uint16_t) * static_cast<size_t>(B) * H,
-                      cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return MTP_ERR_CUDA;
-  void* cat = workspace_bytes >= step_workspace_bytes(B, H) ? static_cast<uint8_t*>(workspace) + step_concat_offset(B)
-                                                             : nullptr;
-  v = run_input(embed, enorm_w, hnorm_w, eh_proj, tokens_dev, hidden_dev, x_dev, status, B, H, V,
-                eps, stream, cat);
-  if (v != MTP_OK) return v;
-  v = run_output(x_dev, final_norm_w, lm_head, row_scale, w_dtype, nullptr, draft_dev, status,
-                 workspace, B, H, V, eps, stream);
-  if (v != MTP_OK) return v;
-  if (cudaMemcpyAsync(draft_host, draft_dev, sizeof(int32_t) * B, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return MTP_ERR_CUDA;
-  int32_t dev_status = 0;
-  if (status && cudaMemcpyAsync(&dev_status, status, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return MTP_ERR_CUDA;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return MTP_ERR_CUDA;
-  return dev_status;
+  HostStep hs{embed, enorm_w, hnorm_w, eh_proj, final_norm_w, lm_head, row_scale, w_dtype, tokens_dev, hidden_dev,
+              x_dev, draft_dev, status, workspace, workspace_bytes, B, H, V, eps, static_cast<cudaStream_t>(stream)};
+  return run_host_step(hs, tokens_host, hidden_host, draft_host);
 }
 
 size_t mtp_head_context_workspace_bytes(int R, int H) {

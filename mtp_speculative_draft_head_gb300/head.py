@@ -93,6 +93,18 @@ class MtpDraftHead:
                                       self.ws, status, self.eps, stream)
         return x, logits, draft
 
+    def host_step(self, B: int = 1, fp8: bool = False, stream=None, status=None) -> "_lib.HostStep":
+        """A prepared synchronous draft step from host buffers (the source's forward_one shape):
+        device buffers for B sequences are allocated here and bound once; call the result with
+        (tokens_host [B] int32, hidden_host [B, H] bf16, draft_host [B] int32), pinned."""
+        W, s, wt = self._head(fp8)
+        dev = self.device
+        return _lib.HostStep(self.embed, self.enorm_w, self.hnorm_w, self.eh_proj, self.final_norm_w, W, s, wt,
+                             torch.empty(B, dtype=torch.int32, device=dev),
+                             torch.empty((B, self.H), dtype=torch.bfloat16, device=dev),
+                             torch.empty((B, self.H), dtype=torch.bfloat16, device=dev),
+                             torch.empty(B, dtype=torch.int32, device=dev), self.ws, status, self.eps, stream)
+
     # ------------------------------------------------------------------ draft chains
     def chain(self, first_tokens, hiddens, fp8: bool = False, graph: bool = True, status=None):
         """Draft ``steps`` tokens per sequence, each step feeding its draft (device-resident) into

@@ -437,3 +437,61 @@ def test_prebuilt_concat_gives_the_same_x(H, B):
     assert int(st.item()) == m.ERR_TOKEN_RANGE
     assert torch.equal(x_fw.view(torch.int16), x_in.view(torch.int16))
     assert bool((x_fw[B // 2].view(torch.int16) == 0).all())
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_host_forward_graph_replays_match_device_path(fp8):
+    """On a non-default stream the host-buffer step runs directly on the first call, then replays
+    a recorded CUDA graph around staging buffers: every call must give the draft the device path
+    gives for its own inputs (fresh host buffers each call), and a bad token must still come back
+    as the returned status."""
+    H, V, B = 256, 4096, 3
+    c = Case(H, V, B, seed=21)
+    head = m.MtpDraftHead(c.g["embed"], c.g["lm_head"], c.g["eh_proj"], c.g["enorm_w"], c.g["hnorm_w"],
+                          c.g["final_norm_w"], eps=EPS, max_batch=B)
+    assert head.quantize_fp8() == 0
+    W, s, wt = head._head(fp8)
+    stream = torch.cuda.Stream()
+    td = torch.empty(B, dtype=torch.int32, device=DEV)
+    hd = torch.empty((B, H), dtype=torch.bfloat16, device=DEV)
+    xd = torch.empty((B, H), dtype=torch.bfloat16, device=DEV)
+    dd = torch.empty(B, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for step in range(5):
+        tokens, hidden = synth.make_step_inputs(H, V, B, 500 + step, "cpu")
+        if step == 4:
+            tokens[1] = V + 1
+        th, hh = tokens.pin_memory(), hidden.pin_memory()
+        dh = torch.full((B,), -9, dtype=torch.int32).pin_memory()
+        args = (head.embed, head.enorm_w, head.hnorm_w, head.eh_proj, head.final_norm_w, W, s, wt, th, hh,
+                td, hd, xd, dd, dh, head.ws, st, EPS, stream)
+        if step < 4:
+            m.mtp_head_forward_host(*args)
+            _, _, draft = head.forward(tokens.to(DEV), hidden.to(DEV), fp8=fp8)
+            torch.cuda.synchronize()
+            assert dh.tolist() == draft.cpu().tolist(), step
+        else:
+            with pytest.raises(m.MTPError) as e:
+                m.mtp_head_forward_host(*args)
+            assert e.value.code == m.ERR_TOKEN_RANGE
+
+
+def test_prepared_host_step_matches_device_path():
+    """MtpDraftHead.host_step binds the device buffers once; each call passes host buffers (as
+    tensors or addresses) and must give the device path's draft."""
+    H, V, B = 512, 3000, 2
+    c = Case(H, V, B, seed=23)
+    head = m.MtpDraftHead(c.g["embed"], c.g["lm_head"], c.g["eh_proj"], c.g["enorm_w"], c.g["hnorm_w"],
+                          c.g["final_norm_w"], eps=EPS, max_batch=B)
+    step = head.host_step(B, stream=torch.cuda.Stream())
+    dh = torch.empty(B, dtype=torch.int32).pin_memory()
+    for i in range(4):
+        tokens, hidden = synth.make_step_inputs(H, V, B, 900 + i, "cpu")
+        th, hh = tokens.pin_memory(), hidden.pin_memory()
+        if i % 2:
+            step(th.data_ptr(), hh.data_ptr(), dh.data_ptr())
+        else:
+            step(th, hh, dh)
+        _, _, draft = head.forward(tokens.to(DEV), hidden.to(DEV))
+        torch.cuda.synchronize()
+        assert dh.tolist() == draft.cpu().tolist()
