@@ -41,7 +41,7 @@ import synth  # noqa: E402
 METRIC = "lm_head draft sweep µs and HBM GB/s (BF16/FP8, H=6144, V=154880, B=1)"
 H, V, B = 6144, 154880, 1
 BATCHES = (2, 4, 8, 16)
-CONTEXT_ROWS = (512, 4096)  # context-row (prefill) batches timed through mtp_head_context_rows
+CONTEXT_ROWS = (17, 64, 128, 256, 512, 1024, 2048, 4096)  # context-row batches timed through mtp_head_context_rows
 EPS = synth.EPS
 CHAIN = 1000
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")

@@ -41,10 +41,12 @@ constexpr int kTcThreads = kTcWarps * 32;          // 384: three warps per SM su
 constexpr int kPrologueThreads = (kConsumerWarps + kBuilderWarps) * 32;  // 352
 constexpr int kTileRows = 16 * kConsumerWarps;     // 128
 // Row tiles per group (their accumulators stay in registers while the activations of a stage
-// are reused across them). With two n-tiles (B > 8) the FP8 activation fragments of a stage
-// take 64 registers, and its groups are 4 tiles.
+// are reused across them). Four: with two n-tiles (B > 8) the FP8 activation fragments of a
+// stage take 64 registers, and measured at H = 6144, V = 154880 groups of 4 were also ~4 us
+// faster than groups of 8 for every other batch and weight type (B = 4, 8: BF16 284 -> 280 us,
+// FP8 153 -> 149 us).
 template <int WT, int NT>
-__host__ __device__ constexpr int tile_group() { return (NT == 2 && WT == MTP_W_FP8_E4M3) ? 4 : 8; }
+__host__ __device__ constexpr int tile_group() { return 4; }
 constexpr int kATileBytes = kTileRows * 128;       // 16 KB: 128 rows x 128 bytes (one k-block)
 // A weight stage holds kKS consecutive k-blocks of one row tile (two tensor loads issued back to
 // back): each row is then read 256 contiguous bytes at a time. With one k-block per visit (128
