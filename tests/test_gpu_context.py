@@ -49,7 +49,7 @@ class Ctx:
         m.mtp_head_context_rows(self.g["embed"], self.g["enorm_w"], self.g["hnorm_w"], self.g["eh_proj"],
                                 self.tokens.to(DEV), self.hidden.to(DEV), x, ws, st, EPS)
         torch.cuda.synchronize()
-        return synth.bits(x), int(st.item()), ws
+        return x, int(st.item()), ws
 
     def oracle(self, rows=None):
         rows = np.arange(self.R) if rows is None else np.asarray(rows)
@@ -61,19 +61,24 @@ class Ctx:
         return x, concat, st, sums
 
 
-def workspace_concat(ws, R, H):
-    """The normalised concat rows the first kernel leaves at the start of the workspace."""
-    return ws[: R * 2 * H * 2].view(torch.int16).view(R, 2 * H).cpu().numpy().view(np.uint16)
+def workspace_concat(ws, R, H, rows):
+    """Rows of the normalised concat the first kernel leaves at the start of the workspace."""
+    idx = torch.as_tensor(rows, dtype=torch.long, device=ws.device)
+    return ws[: R * 2 * H * 2].view(torch.int16).view(R, 2 * H)[idx].cpu().numpy().view(np.uint16)
+
+
+def x_rows(x, rows):
+    return synth.bits(x[torch.as_tensor(rows, dtype=torch.long, device=x.device)])
 
 
 def check_rows(c, x_gpu, ws, rows=None):
     rows = np.arange(c.R) if rows is None else np.asarray(rows)
     x_ref, concat_ref, st_ref, sums = c.oracle(rows)
     ok = st_ref == 0
-    assert np.array_equal(workspace_concat(ws, c.R, c.H)[rows][ok], concat_ref[ok]), "concat differs from the oracle"
+    assert np.array_equal(workspace_concat(ws, c.R, c.H, rows)[ok], concat_ref[ok]), "concat differs from the oracle"
     abs_sums = abs_product_sums(c.wb["eh_proj"], concat_ref)
     K = 2 * c.H
-    x_sel = x_gpu[rows]
+    x_sel = x_rows(x_gpu, rows)
     assert np.all(x_sel[~ok] == 0), "rows with an out-of-range token must be zeros"
     diff = np.nonzero(x_sel[ok] != x_ref[ok])[0].size
     # the FP32-accumulation band, as an interval check around the exact sum
@@ -144,6 +149,7 @@ def test_context_rows_small_r_is_batched_input():
     c = Ctx(H, R, seed=5)
     x, st, _ = c.run()
     assert st == 0
+    x = synth.bits(x)
     xb = torch.full((R, H), 7, dtype=torch.bfloat16, device=DEV)
     stb = torch.zeros(1, dtype=torch.int32, device=DEV)
     m.mtp_head_input_batched(c.g["embed"], c.g["enorm_w"], c.g["hnorm_w"], c.g["eh_proj"], c.tokens.to(DEV),
@@ -156,7 +162,7 @@ def test_context_rows_deterministic_and_workspace_checked():
     c = Ctx(512, 200, seed=9)
     x1, _, _ = c.run()
     x2, _, _ = c.run(ws_extra=4096)
-    assert np.array_equal(x1, x2)
+    assert torch.equal(x1.view(torch.int16), x2.view(torch.int16))
     small = torch.empty(m.mtp_head_context_workspace_bytes(200, 512) - 1, dtype=torch.uint8, device=DEV)
     x = torch.empty((200, 512), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(m.MTPError) as e:
@@ -170,3 +176,28 @@ def test_context_rows_deterministic_and_workspace_checked():
         m.mtp_head_context_rows(c2.g["embed"], c2.g["enorm_w"], c2.g["hnorm_w"], c2.g["eh_proj"],
                                 c2.tokens.to(DEV), c2.hidden.to(DEV), x, ws)
     assert e.value.code == m.ERR_NOT_IMPLEMENTED
+
+
+def test_context_rows_maximum_rows_sampled():
+    """The largest R the entry point takes (65536) at the GLM hidden size: 6080 whole tiles in 40
+    waves and the split remainder; the oracle checks rows at both ends and across tiles."""
+    H, R = 6144, 65536
+    V = 4096
+    c = Ctx(H, R, V=V, seed=77)
+    x, st, ws = c.run()
+    assert st == 0
+    check_rows(c, x, ws, rows=[0, 255, 256, 30001, 65279, 65280, 65535])
+
+
+def test_context_rows_smallest_gemm_shape_and_all_tokens_invalid():
+    # H = 32: one 64-element k-block per half, a single partial column tile
+    c = Ctx(32, 17, V=50, seed=4)
+    x, st, ws = c.run()
+    assert st == 0
+    check_rows(c, x, ws)
+    # every token out of range: all rows zero, status set, nothing else read from embed
+    c2 = Ctx(256, 40, V=100, seed=6)
+    c2.tokens = torch.full((40,), 100, dtype=torch.int32)
+    x2, st2, _ = c2.run()
+    assert st2 == m.ERR_TOKEN_RANGE
+    assert bool((x2.view(torch.int16) == 0).all())
