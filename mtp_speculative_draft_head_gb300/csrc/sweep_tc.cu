@@ -9,15 +9,16 @@
 // be widened straight into A fragments by the hardware E4M3 -> f16 conversion, with no trip
 // through shared memory.
 //
-// Roles (416 threads):
-//  * producer warp: streams 128-row x 128-byte tiles of lm_head with 2-D TMA tensor loads
-//    (128-byte swizzle) into a 12-stage ring (mbarrier full/empty pairs, bounded waits);
-//  * 4 builder warps: compute xhat = rms_norm_vanilla(x, final_norm_w) one k-block at a time
+// Roles (384 threads, 12 warps: up to 168 registers a thread):
+//  * producer warp: streams 128-row tiles of lm_head, two 128-byte k-blocks per row and stage,
+//    with 2-D TMA tensor loads (128-byte swizzle) into a 6-stage ring of 32 KB (mbarrier
+//    full/empty pairs, bounded waits);
+//  * 3 builder warps: compute xhat = rms_norm_vanilla(x, final_norm_w) one stage at a time
 //    (BF16 for a BF16 head; for FP8, f16 scaled by 2^k per sequence, exact) into a small ring, in
 //    the same swizzled layout, with the same exact rounding as the other kernels;
 //  * 8 consumer warps: 16 rows each of a 128-row tile; ldmatrix + mma.sync, batch as N (8 or 16).
-// Loop order: groups of up to 8 row tiles; per k-block the activations are built once and used by
-// every tile of the group, whose accumulators stay in registers. Each lm_head byte is read once.
+// Loop order: groups of 4 row tiles; per stage the activations are built once and used by every
+// tile of the group, whose accumulators stay in registers. Each lm_head byte is read once.
 // FP8 A fragments come out of ldmatrix with four codes per register; with k permuted the same way
 // in the activations (codes 4t..4t+3 of a 16-code block sit in k slots 2t, 2t+1, 2t+8, 2t+9 of
 // thread t) every product pairs the right code with the right activation.
