@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
     for name in ("mtp_head_input", "mtp_head_input_batched", "mtp_head_logits_argmax",
                  "mtp_head_logits_argmax_batched", "mtp_head_quantize_fp8",
                  "mtp_head_workspace_bytes", "mtp_head_forward_batched", "mtp_head_forward_host",
-                 "mtp_head_strerror"):
+                 "mtp_head_context_rows", "mtp_head_context_workspace_bytes",
+                 "mtp_head_logits_argmax_batched_noalloc", "mtp_head_strerror"):
         assert name in d
 
 
@@ -61,6 +62,17 @@ def test_workspace_bytes(lib):
     assert m.mtp_head_workspace_bytes(0, 6144, 154880) == 0
     assert m.mtp_head_workspace_bytes(17, 6144, 154880) == 0
     assert m.mtp_head_workspace_bytes(1, 0, 10) == 0
+    # the whole-step workspace also has room for the batched input stage's prebuilt concat
+    assert m.mtp_head_workspace_bytes(16, 6144, 154880) >= 128 + 8192 * 16 + 16 * 2 * 6144 * 2 + 16 * 4
+
+
+def test_context_workspace_bytes(lib):
+    f = m.mtp_head_context_workspace_bytes
+    assert f(0, 6144) == 0 and f(65537, 6144) == 0 and f(17, 0) == 0 and f(17, 65537) == 0
+    for R, H in ((17, 32), (512, 6144), (65536, 6144)):
+        assert f(R, H) >= R * 2 * H * 2 + R * 4  # the concat and the row flags, at least
+    sizes = [f(R, 1024) for R in (17, 100, 256, 257, 4096)]
+    assert sizes == sorted(sizes)
 
 
 A = 0x10000  # an aligned fake device address (never dereferenced)
@@ -146,3 +158,39 @@ def test_forward_host_validation(lib):
     bad = list(args)
     bad[18] = 0  # B
     assert f(*bad) == m.ERR_SHAPE
+
+
+def _context(lib, **kw):
+    args = dict(embed=A, enorm_w=A, hnorm_w=A, eh_proj=A, tokens=A, hidden=A, x=A, status=None, ws=A,
+                ws_bytes=1 << 30, R=300, H=256, V=100, eps=1e-6)
+    args.update(kw)
+    return lib.mtp_head_context_rows(args["embed"], args["enorm_w"], args["hnorm_w"], args["eh_proj"],
+                                     args["tokens"], args["hidden"], args["x"], args["status"], args["ws"],
+                                     args["ws_bytes"], args["R"], args["H"], args["V"], args["eps"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(embed=None), m.ERR_ARG),
+    (dict(eh_proj=None), m.ERR_ARG),
+    (dict(tokens=None), m.ERR_ARG),
+    (dict(x=None), m.ERR_ARG),
+    (dict(eps=float("nan")), m.ERR_ARG),
+    (dict(R=0), m.ERR_SHAPE),
+    (dict(R=65537), m.ERR_SHAPE),
+    (dict(H=0), m.ERR_SHAPE),
+    (dict(V=0), m.ERR_SHAPE),
+    (dict(x=A + 8), m.ERR_ALIGN),
+    (dict(tokens=A + 2), m.ERR_ALIGN),
+    (dict(ws=A + 8), m.ERR_ALIGN),
+    (dict(H=100), m.ERR_NOT_IMPLEMENTED),  # R > 16 runs the GEMM, which needs H % 32 == 0
+    (dict(ws=None), m.ERR_WORKSPACE),
+    (dict(ws_bytes=1024), m.ERR_WORKSPACE),
+])
+def test_context_rows_validation(lib, kw, code):
+    assert _context(lib, **kw) == code
+
+
+def test_noalloc_output_stage_validation(lib):
+    f = lib.mtp_head_logits_argmax_batched_noalloc
+    assert f(A, A, A, None, m.W_BF16, None, A, None, 0, 64, 100, ctypes.c_float(1e-6), None) == m.ERR_SHAPE
+    assert f(A, A, A, None, m.W_BF16, None, A, None, 17, 64, 100, ctypes.c_float(1e-6), None) == m.ERR_SHAPE
