@@ -82,8 +82,8 @@ __global__ void __launch_bounds__(kCtxNormThreads) context_concat_rows_kernel(co
 // Many rows (bandwidth-bound): one warp per normalised vector (vector 2r: enorm of the embedding
 // row of tokens[r]; 2r + 1: hnorm of hidden row r), no block-level synchronisation, many vectors
 // in flight per SM. Pass 1 reads x in batches of kCatBatch 16-byte pieces per lane (all in
-// flight together) into four independent double-float sums; pass 2 reads x again (L1 / L2) with
-// the norm weight, again a batch at a time.
+// flight together) into four packed pairs of double-float sums; pass 2 reads x again (L1 / L2)
+// with the norm weight, again a batch at a time.
 constexpr int kCatWarps = 8;
 constexpr int kCatBatch = 8;
 
@@ -119,7 +119,11 @@ __global__ void __launch_bounds__(kCatWarps * 32, 4) context_concat_warps_kernel
       for (int v = lane; v < nv8; v += 32) out[v] = z;
       continue;
     }
-    DF acc[4] = {DF{0.0f, 0.0f}, DF{0.0f, 0.0f}, DF{0.0f, 0.0f}, DF{0.0f, 0.0f}};
+    // four packed pairs of double-float sums (f32x2: two TwoSums per instruction sequence);
+    // each square of a BF16 value is exact in fp32
+    DF2 acc[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) acc[t] = DF2{0ull, 0ull};
     for (int v0 = 0; v0 < nv8; v0 += 32 * kCatBatch) {
       uint4 q[kCatBatch];
 #pragma unroll
@@ -132,13 +136,13 @@ __global__ void __launch_bounds__(kCatWarps * 32, 4) context_concat_warps_kernel
         const uint32_t u[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          const float lo = bf16_lo(u[t]), hi = bf16_hi(u[t]);
-          df_add(acc[t], __fmul_rn(lo, lo));
-          df_add(acc[t], __fmul_rn(hi, hi));
+          const uint64_t x2 = bf16x2_to_f2(u[t]);
+          df2_add(acc[t], f2_mul(x2, x2));
         }
       }
     }
-    DF tot = df_add(df_add(acc[0], acc[1]), df_add(acc[2], acc[3]));
+    DF tot = df_add(df_add(df_add(df2_x(acc[0]), df2_y(acc[0])), df_add(df2_x(acc[1]), df2_y(acc[1]))),
+                    df_add(df_add(df2_x(acc[2]), df2_y(acc[2])), df_add(df2_x(acc[3]), df2_y(acc[3]))));
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) tot = df_add(tot, shfl_xor_df(tot, m));
     const double ms = (static_cast<double>(tot.hi) + static_cast<double>(tot.lo)) * a.inv_h;
