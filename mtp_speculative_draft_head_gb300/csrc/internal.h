@@ -131,8 +131,6 @@ cudaError_t launch_sweep(const SweepArgs& a, cudaStream_t stream);
 // Batched (2 <= B <= 16) output stage on tensor cores; *launched stays false when the shape is
 // not supported (H not a multiple of 8, no tensor-map encoder, not enough shared memory).
 cudaError_t launch_sweep_tc(const SweepArgs& a, cudaStream_t stream, bool* launched);
-// The same on tcgen05 (TMEM accumulators); *launched stays false when the shape is not supported.
-cudaError_t launch_sweep_umma(const SweepArgs& a, cudaStream_t stream, bool* launched);
 cudaError_t launch_quantize(const uint16_t* w, uint8_t* q, float* scale, int32_t* status,
                             int V, int H, cudaStream_t stream);
 

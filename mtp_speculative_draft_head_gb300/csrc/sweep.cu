@@ -734,8 +734,6 @@ cudaError_t launch_sweep(const SweepArgs& in, cudaStream_t stream) {
   }
   if (a.B >= MTP_TC_MIN_B) {
     bool launched = false;
-    err = launch_sweep_umma(a, stream, &launched);
-    if (launched || err != cudaSuccess) return err;
     err = launch_sweep_tc(a, stream, &launched);
     if (launched || err != cudaSuccess) return err;
   }
