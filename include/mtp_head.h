@@ -215,10 +215,12 @@ int mtp_head_forward_batched(const uint16_t* embed, const uint16_t* enorm_w,
  *
  * On a stream other than the legacy default stream (and not under the caller's own capture),
  * the first call for a given set of device buffers, shapes, eps and stream runs operation by
- * operation and then records the step in a CUDA graph around small pinned staging buffers
- * (held by the library, at most 8 such steps, least recently used replaced). Later calls with
- * the same set copy the host inputs into the staging buffers, launch the graph once, wait, and
- * copy the draft out: the same work, without a launch per operation. The host buffers may
+ * operation and then records the step in a CUDA graph around small mapped pinned staging
+ * buffers (held by the library, at most 8 such steps, least recently used replaced). Later calls
+ * with the same set copy the host inputs into the staging buffers, launch the graph once, wait,
+ * and copy the draft out: the same work, without a launch per operation. Inside the graph the
+ * moves between the staging buffers and tokens_dev / hidden_dev / draft_dev are small kernels
+ * on the mapped memory (when B * H is a multiple of 8; copy operations otherwise). The host buffers may
  * differ from call to call. Calls from several threads are safe; calls sharing a recorded
  * step are serialised.
  * ---------------------------------------------------------------------------------------- */

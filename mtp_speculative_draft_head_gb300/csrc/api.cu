@@ -219,15 +219,41 @@ std::shared_ptr<StepGraph> record_step(const HostStep& s, int device) {
   const size_t hid_bytes = sizeof(uint16_t) * static_cast<size_t>(s.B) * s.H;
   const size_t tok_bytes = (sizeof(int32_t) * s.B + 15) / 16 * 16;
   uint8_t* base = nullptr;
-  if (cudaHostAlloc(reinterpret_cast<void**>(&base), 2 * tok_bytes + 16 + hid_bytes, cudaHostAllocDefault) !=
-      cudaSuccess)
+  if (cudaHostAlloc(reinterpret_cast<void**>(&base), 2 * tok_bytes + 16 + hid_bytes,
+                    cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess)
     return nullptr;
   g->tok = reinterpret_cast<int32_t*>(base);
   g->draft = reinterpret_cast<int32_t*>(base + tok_bytes);
   g->st = reinterpret_cast<int32_t*>(base + 2 * tok_bytes);
   g->hid = reinterpret_cast<uint16_t*>(base + 2 * tok_bytes + 16);
+  // the device's view of the staging buffers: the moves in and out are kernels reading and
+  // writing them directly (whole 16-byte pieces of hidden rows); otherwise copy operations
+  uint8_t* dbase = nullptr;
+  const bool kernel_io = (static_cast<size_t>(s.B) * s.H) % 8 == 0 &&
+                         cudaHostGetDevicePointer(reinterpret_cast<void**>(&dbase), base, 0) == cudaSuccess;
+  if (!kernel_io) cudaGetLastError();
   if (cudaStreamBeginCapture(s.stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return nullptr;
-  const int v = enqueue_host_step(s, g->tok, g->hid, g->draft, g->st);
+  int v = MTP_OK;
+  if (kernel_io) {
+    v = map_cuda(mtp::launch_host_in(reinterpret_cast<const int32_t*>(dbase),
+                                     reinterpret_cast<const uint16_t*>(dbase + 2 * tok_bytes + 16), s.tokens_dev,
+                                     s.hidden_dev, s.B, s.H, s.stream));
+    if (v == MTP_OK) {
+      void* cat = s.workspace_bytes >= step_workspace_bytes(s.B, s.H)
+                      ? static_cast<uint8_t*>(s.workspace) + step_concat_offset(s.B)
+                      : nullptr;
+      v = run_input(s.embed, s.enorm_w, s.hnorm_w, s.eh_proj, s.tokens_dev, s.hidden_dev, s.x_dev, s.status, s.B,
+                    s.H, s.V, s.eps, s.stream, cat);
+    }
+    if (v == MTP_OK)
+      v = run_output(s.x_dev, s.final_norm_w, s.lm_head, s.row_scale, s.w_dtype, nullptr, s.draft_dev, s.status,
+                     s.workspace, s.B, s.H, s.V, s.eps, s.stream);
+    if (v == MTP_OK)
+      v = map_cuda(mtp::launch_host_out(s.draft_dev, reinterpret_cast<int32_t*>(dbase + tok_bytes), s.status,
+                                        reinterpret_cast<int32_t*>(dbase + 2 * tok_bytes), s.B, s.stream));
+  } else {
+    v = enqueue_host_step(s, g->tok, g->hid, g->draft, g->st);
+  }
   cudaGraph_t graph = nullptr;
   const cudaError_t e = cudaStreamEndCapture(s.stream, &graph);
   if (v != MTP_OK || e != cudaSuccess || graph == nullptr) {

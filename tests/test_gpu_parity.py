@@ -439,13 +439,14 @@ def test_prebuilt_concat_gives_the_same_x(H, B):
     assert bool((x_fw[B // 2].view(torch.int16) == 0).all())
 
 
+@pytest.mark.parametrize("H,B", [(256, 3), (100, 1)])  # moves as kernels; B * H % 8 != 0: copy operations
 @pytest.mark.parametrize("fp8", [False, True])
-def test_host_forward_graph_replays_match_device_path(fp8):
+def test_host_forward_graph_replays_match_device_path(fp8, H, B):
     """On a non-default stream the host-buffer step runs directly on the first call, then replays
-    a recorded CUDA graph around staging buffers: every call must give the draft the device path
-    gives for its own inputs (fresh host buffers each call), and a bad token must still come back
-    as the returned status."""
-    H, V, B = 256, 4096, 3
+    a recorded CUDA graph around mapped staging buffers: every call must give the draft the device
+    path gives for its own inputs (fresh host buffers each call), and a bad token must still come
+    back as the returned status."""
+    V = 4096
     c = Case(H, V, B, seed=21)
     head = m.MtpDraftHead(c.g["embed"], c.g["lm_head"], c.g["eh_proj"], c.g["enorm_w"], c.g["hnorm_w"],
                           c.g["final_norm_w"], eps=EPS, max_batch=B)
@@ -460,7 +461,7 @@ def test_host_forward_graph_replays_match_device_path(fp8):
     for step in range(5):
         tokens, hidden = synth.make_step_inputs(H, V, B, 500 + step, "cpu")
         if step == 4:
-            tokens[1] = V + 1
+            tokens[B - 1] = V + 1
         th, hh = tokens.pin_memory(), hidden.pin_memory()
         dh = torch.full((B,), -9, dtype=torch.int32).pin_memory()
         args = (head.embed, head.enorm_w, head.hnorm_w, head.eh_proj, head.final_norm_w, W, s, wt, th, hh,
