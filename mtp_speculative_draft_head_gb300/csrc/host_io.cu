@@ -15,13 +15,24 @@ namespace mtp {
 namespace {
 
 constexpr int kIoThreads = 256;
+constexpr int kIoPer = 4;  // 16-byte pieces a thread has in flight at once (host memory is far away)
 
-__global__ void __launch_bounds__(kIoThreads) host_in_kernel(const int32_t* tok_src, const uint4* hid_src,
-                                                              int32_t* tok_dst, uint4* hid_dst, int B, int n16) {
+// Grid: ceil(n16 / (kIoThreads * kIoPer)) CTAs; CTA 0 also moves the tokens (B <= 16).
+__global__ void __launch_bounds__(kIoThreads) host_in_kernel(const int32_t* __restrict__ tok_src,
+                                                              const uint4* __restrict__ hid_src,
+                                                              int32_t* __restrict__ tok_dst,
+                                                              uint4* __restrict__ hid_dst, int B, int n16) {
   pdl_wait_prior_grid();
   pdl_launch_dependents();  // the input stage may start its weight stream now
-  for (int i = threadIdx.x; i < n16; i += kIoThreads) hid_dst[i] = hid_src[i];
-  if (threadIdx.x < B) tok_dst[threadIdx.x] = tok_src[threadIdx.x];
+  const int base = blockIdx.x * kIoThreads * kIoPer + threadIdx.x;
+  uint4 v[kIoPer];
+#pragma unroll
+  for (int j = 0; j < kIoPer; ++j)
+    if (base + j * kIoThreads < n16) v[j] = hid_src[base + j * kIoThreads];
+#pragma unroll
+  for (int j = 0; j < kIoPer; ++j)
+    if (base + j * kIoThreads < n16) hid_dst[base + j * kIoThreads] = v[j];
+  if (blockIdx.x == 0 && threadIdx.x < B) tok_dst[threadIdx.x] = tok_src[threadIdx.x];
 }
 
 __global__ void __launch_bounds__(32) host_out_kernel(const int32_t* draft_src, int32_t* draft_dst,
@@ -43,7 +54,9 @@ cudaError_t launch_host_in(const int32_t* tok_src, const uint16_t* hid_src, int3
   const void* src = hid_src;
   void* dst = hid_dst;
   void* params[] = {&tok_src, &src, &tok_dst, &dst, &B, &n16};
-  return launch_pdl(reinterpret_cast<const void*>(host_in_kernel), dim3(1), dim3(kIoThreads), 0, stream, params);
+  const int grid = (n16 + kIoThreads * kIoPer - 1) / (kIoThreads * kIoPer);
+  return launch_pdl(reinterpret_cast<const void*>(host_in_kernel), dim3(grid > 0 ? grid : 1), dim3(kIoThreads), 0,
+                    stream, params);
 }
 
 cudaError_t launch_host_out(const int32_t* draft_src, int32_t* draft_dst, const int32_t* status_src, int32_t* status_dst,
