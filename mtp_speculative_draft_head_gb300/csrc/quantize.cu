@@ -5,8 +5,19 @@
 //   q[v, k] = e4m3_rne_satfinite( fp32( w[v, k] / s[v] ) )     (s = 0: all codes 0)
 // Both divisions are IEEE round-to-nearest (no fast-math in this file), and the E4M3 rounding
 // is the hardware conversion with satfinite, so the codes are a pure function of the input.
-// Run once per weight load, not per draft: one warp per row, two passes over the row.
-#include <cuda_fp8.h>
+// Run once per weight load, not per draft: one warp per row, two passes over the row (the
+// second from L2), with several 16-byte loads in flight per lane in each.
+//
+// The codes without a division per element. The code of the quotient depends only on which
+// pair of neighbouring E4M3 rounding boundaries the quotient lies between. With r = 1/s, the
+// products y_up = f * r (1 + 2^-21) and y_dn = f * r (1 - 2^-21) (each factor and product
+// rounded to nearest) bracket fp32(f / s) strictly: the four roundings move them by at most
+// 3 * 2^-24 relative, fp32(f / s) is within 2^-24 of f / s, and 2^-21 - 3 * 2^-24 > 2^-24.
+// The conversion to E4M3 (round to nearest even, saturating) is monotonic, so when y_up and
+// y_dn give the same code, fp32(f / s) gives it too. Otherwise (a boundary inside the bracket,
+// probability ~1e-5 per element) the code comes from the division itself. Quotients below the
+// fp32 normal range convert to a signed zero on all three paths. Rows whose scale is not a
+// normal fp32 number take the division for every element.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,81 +28,140 @@ namespace mtp {
 
 namespace {
 
-__device__ __forceinline__ uint8_t e4m3_of(float q) {
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3));
+constexpr int kQThreads = 256;
+constexpr int kLoadsMag = 8;     // 16-byte loads in flight per lane, magnitude pass
+constexpr int kPiecesCode = 4;   // 16-element pieces (32 bytes in, 16 out) in flight per lane
+
+// Two E4M3 codes (round to nearest even, satfinite): byte 0 from lo, byte 1 from hi.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
 }
 
-__global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ w,
-                                                       uint8_t* __restrict__ q,
-                                                       float* __restrict__ scale,
-                                                       int32_t* __restrict__ status, int64_t V,
-                                                       int H) {
+// max of the two 16-bit halves, lane by lane
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Codes of one bf16 pair (32-bit word) through the bracket, the division when it is open.
+__device__ __forceinline__ uint32_t pair_codes(uint32_t pair, float s, float r_up, float r_dn) {
+  const float a = bf16_lo(pair), b = bf16_hi(pair);
+  const uint32_t up = e4m3x2(__fmul_rn(a, r_up), __fmul_rn(b, r_up));
+  const uint32_t dn = e4m3x2(__fmul_rn(a, r_dn), __fmul_rn(b, r_dn));
+  if (up == dn) return up;
+  return e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+}
+
+__device__ __forceinline__ uint32_t pair_codes_div(uint32_t pair, float s) {
+  return e4m3x2(__fdiv_rn(bf16_lo(pair), s), __fdiv_rn(bf16_hi(pair), s));
+}
+
+// Rows with H % 16 == 0: 16-byte loads and stores.
+__global__ void __launch_bounds__(kQThreads) quantize_vec_kernel(const uint16_t* __restrict__ w,
+                                                                 uint8_t* __restrict__ q,
+                                                                 float* __restrict__ scale,
+                                                                 int32_t* __restrict__ status,
+                                                                 int64_t V, int H) {
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t tw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const bool vec = (H & 15) == 0;
+  const int n8 = H >> 3;    // 16-byte words of a row
+  const int n16 = H >> 4;   // 16-element pieces of a row
   for (int64_t v = gw; v < V; v += tw) {
-    const uint16_t* row = w + v * H;
-    uint8_t* qrow = q + v * H;
+    const uint4* rv = reinterpret_cast<const uint4*>(w + v * H);
     // pass 1: magnitude maximum on the bit patterns (|x| order == (bits & 0x7FFF) order for
-    // finite BF16) and a non-finite flag
-    uint32_t mx = 0, bad = 0;
-    if (vec) {
-      const uint4* rv = reinterpret_cast<const uint4*>(row);
-      for (int j = lane; j < H / 8; j += 32) {
-        const uint4 u = rv[j];
-        const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
+    // finite BF16; NaN and Inf have the largest patterns, so they show in the maximum)
+    uint32_t mx2 = 0;
+    for (int b = 0; b < n8; b += 32 * kLoadsMag) {
+      uint4 u[kLoadsMag];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const uint32_t lo = ws[t] & 0x7FFFu, hi = (ws[t] >> 16) & 0x7FFFu;
-          bad |= ((lo & 0x7F80u) == 0x7F80u) | ((hi & 0x7F80u) == 0x7F80u);
-          mx = max(mx, max(lo, hi));
-        }
+      for (int i = 0; i < kLoadsMag; ++i) {
+        const int j = b + 32 * i + lane;
+        u[i] = j < n8 ? rv[j] : make_uint4(0u, 0u, 0u, 0u);
       }
-    } else {
-      for (int k = lane; k < H; k += 32) {
-        const uint32_t m = row[k] & 0x7FFFu;
-        bad |= (m & 0x7F80u) == 0x7F80u;
-        mx = max(mx, m);
+#pragma unroll
+      for (int i = 0; i < kLoadsMag; ++i) {
+        mx2 = max_u16x2(mx2, u[i].x & 0x7FFF7FFFu);
+        mx2 = max_u16x2(mx2, u[i].y & 0x7FFF7FFFu);
+        mx2 = max_u16x2(mx2, u[i].z & 0x7FFF7FFFu);
+        mx2 = max_u16x2(mx2, u[i].w & 0x7FFF7FFFu);
       }
     }
+    uint32_t mx = max(mx2 & 0xFFFFu, mx2 >> 16);
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1) {
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-      bad |= __shfl_xor_sync(0xffffffffu, bad, m);
-    }
+    for (int m = 16; m > 0; m >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, m));
     float s = __fdiv_rn(bf16_bits_to_f32(mx), 448.0f);
-    if (bad) {
+    if (mx >= 0x7F80u) {  // a NaN or Inf in the row
       if (lane == 0) store_status(status, MTP_ERR_NONFINITE);
       s = 0.0f;
     }
     if (lane == 0) scale[v] = s;
     // pass 2: codes
-    if (vec) {
-      const uint4* rv = reinterpret_cast<const uint4*>(row);
-      uint4* qv = reinterpret_cast<uint4*>(qrow);
-      for (int j = lane; j < H / 16; j += 32) {
-        const uint4 u0 = rv[2 * j], u1 = rv[2 * j + 1];
-        const uint32_t ws[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        uint32_t out[4];
+    uint4* qv = reinterpret_cast<uint4*>(q + v * H);
+    const bool bracket = s >= 1.17549435e-38f;  // a normal scale: 1/s is finite and exact to 2^-24
+    const float r = bracket ? __frcp_rn(s) : 0.0f;
+    const float r_up = __fmul_rn(r, 1.0f + 0x1p-21f), r_dn = __fmul_rn(r, 1.0f - 0x1p-21f);
+    for (int b = 0; b < n16; b += 32 * kPiecesCode) {
+      uint4 u0[kPiecesCode], u1[kPiecesCode];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          uint32_t word = 0;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t pair = ws[2 * t + h];
-            const uint32_t c0 = (s == 0.0f) ? 0u : e4m3_of(__fdiv_rn(bf16_lo(pair), s));
-            const uint32_t c1 = (s == 0.0f) ? 0u : e4m3_of(__fdiv_rn(bf16_hi(pair), s));
-            word |= (c0 | (c1 << 8)) << (16 * h);
-          }
-          out[t] = word;
+      for (int i = 0; i < kPiecesCode; ++i) {
+        const int j = b + 32 * i + lane;
+        if (j < n16) {
+          u0[i] = __ldcs(rv + 2 * j);
+          u1[i] = __ldcs(rv + 2 * j + 1);
         }
-        qv[j] = make_uint4(out[0], out[1], out[2], out[3]);
       }
-    } else {
-      for (int k = lane; k < H; k += 32)
-        qrow[k] = (s == 0.0f) ? uint8_t(0) : e4m3_of(__fdiv_rn(bf16_bits_to_f32(row[k]), s));
+#pragma unroll
+      for (int i = 0; i < kPiecesCode; ++i) {
+        const int j = b + 32 * i + lane;
+        if (j >= n16) continue;
+        const uint32_t ws[8] = {u0[i].x, u0[i].y, u0[i].z, u0[i].w, u1[i].x, u1[i].y, u1[i].z, u1[i].w};
+        uint32_t c[8];
+        if (s == 0.0f) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) c[t] = 0u;
+        } else if (bracket) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) c[t] = pair_codes(ws[t], s, r_up, r_dn);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) c[t] = pair_codes_div(ws[t], s);
+        }
+        __stcs(qv + j, make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16),
+                                  c[6] | (c[7] << 16)));
+      }
     }
+  }
+}
+
+// Any H: one element at a time.
+__global__ void __launch_bounds__(kQThreads) quantize_scalar_kernel(const uint16_t* __restrict__ w,
+                                                                    uint8_t* __restrict__ q,
+                                                                    float* __restrict__ scale,
+                                                                    int32_t* __restrict__ status,
+                                                                    int64_t V, int H) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t tw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t v = gw; v < V; v += tw) {
+    const uint16_t* row = w + v * H;
+    uint8_t* qrow = q + v * H;
+    uint32_t mx = 0;
+    for (int k = lane; k < H; k += 32) mx = max(mx, static_cast<uint32_t>(row[k]) & 0x7FFFu);
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+    float s = __fdiv_rn(bf16_bits_to_f32(mx), 448.0f);
+    if (mx >= 0x7F80u) {
+      if (lane == 0) store_status(status, MTP_ERR_NONFINITE);
+      s = 0.0f;
+    }
+    if (lane == 0) scale[v] = s;
+    for (int k = lane; k < H; k += 32)
+      qrow[k] = (s == 0.0f) ? uint8_t(0)
+                            : static_cast<uint8_t>(e4m3x2(__fdiv_rn(bf16_bits_to_f32(row[k]), s), 0.0f));
   }
 }
 
@@ -102,16 +172,20 @@ cudaError_t launch_quantize(const uint16_t* w, uint8_t* q, float* scale, int32_t
   DeviceInfo di;
   cudaError_t err = device_info(&di);
   if (err != cudaSuccess) return err;
+  const bool vec = (H & 15) == 0;
+  const void* kern = vec ? reinterpret_cast<const void*>(quantize_vec_kernel)
+                         : reinterpret_cast<const void*>(quantize_scalar_kernel);
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kQThreads, 0);
+  if (err != cudaSuccess) return err;
   const int64_t warps_wanted = V;
-  int64_t blocks = (warps_wanted + 7) / 8;
-  const int64_t cap = static_cast<int64_t>(di.sm_count) * 8;
+  int64_t blocks = (warps_wanted + kQThreads / 32 - 1) / (kQThreads / 32);
+  const int64_t cap = static_cast<int64_t>(di.sm_count) * (per_sm > 0 ? per_sm : 1);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, quantize_kernel, w, q, scale, status, static_cast<int64_t>(V), H);
+  int64_t V64 = V;
+  void* args[] = {&w, &q, &scale, &status, &V64, &H};
+  return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(blocks)), dim3(kQThreads), args, 0, stream);
 }
 
 }  // namespace mtp
