@@ -6,7 +6,7 @@
 // Both divisions are IEEE round-to-nearest (no fast-math in this file), and the E4M3 rounding
 // is the hardware conversion with satfinite, so the codes are a pure function of the input.
 // Run once per weight load, not per draft: one warp per row, two passes over the row (the
-// second from L2), with several 16-byte loads in flight per lane in each.
+// second from L2), with several 16-byte loads in flight per lane in the first.
 //
 // The codes without a division per element. The code of the quotient depends only on which
 // pair of neighbouring E4M3 rounding boundaries the quotient lies between. With r = 1/s, the
@@ -14,8 +14,9 @@
 // rounded to nearest) bracket fp32(f / s) strictly: the four roundings move them by at most
 // 3 * 2^-24 relative, fp32(f / s) is within 2^-24 of f / s, and 2^-21 - 3 * 2^-24 > 2^-24.
 // The conversion to E4M3 (round to nearest even, saturating) is monotonic, so when y_up and
-// y_dn give the same code, fp32(f / s) gives it too. Otherwise (a boundary inside the bracket,
-// probability ~1e-5 per element) the code comes from the division itself. Quotients below the
+// y_dn give the same code, fp32(f / s) gives it too. Otherwise (a boundary inside the bracket:
+// nearly always an exact tie, about 0.5 % of the elements of Gaussian rows) the code comes from
+// the division itself. Quotients below the
 // fp32 normal range convert to a signed zero on all three paths. Rows whose scale is not a
 // normal fp32 number take the division for every element.
 #include <cuda_runtime.h>
@@ -29,8 +30,20 @@ namespace mtp {
 namespace {
 
 constexpr int kQThreads = 256;
-constexpr int kLoadsMag = 8;     // 16-byte loads in flight per lane, magnitude pass
-constexpr int kPiecesCode = 4;   // 16-element pieces (32 bytes in, 16 out) in flight per lane
+// Measured at H = 6144, V = 154880 (best of 7 runs): 4 loads, 1 piece, 6 blocks per SM (40
+// registers, 48 warps per SM) 517 us; 8 / 2 / 4 blocks 524 us; 8 / 4 / no minimum (75 registers)
+// 598 us; 16 / 8 / no minimum 1687 us. More warps beat more loads in flight per warp.
+#ifndef MTP_Q_LOADS
+#define MTP_Q_LOADS 4
+#endif
+#ifndef MTP_Q_PIECES
+#define MTP_Q_PIECES 1
+#endif
+#ifndef MTP_Q_MINB
+#define MTP_Q_MINB 6
+#endif
+constexpr int kLoadsMag = MTP_Q_LOADS;     // 16-byte loads in flight per lane, magnitude pass
+constexpr int kPiecesCode = MTP_Q_PIECES;  // 16-element pieces (32 bytes in, 16 out) per lane and step
 
 // Two E4M3 codes (round to nearest even, satfinite): byte 0 from lo, byte 1 from hi.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
@@ -60,7 +73,7 @@ __device__ __forceinline__ uint32_t pair_codes_div(uint32_t pair, float s) {
 }
 
 // Rows with H % 16 == 0: 16-byte loads and stores.
-__global__ void __launch_bounds__(kQThreads) quantize_vec_kernel(const uint16_t* __restrict__ w,
+__global__ void __launch_bounds__(kQThreads, MTP_Q_MINB) quantize_vec_kernel(const uint16_t* __restrict__ w,
                                                                  uint8_t* __restrict__ q,
                                                                  float* __restrict__ scale,
                                                                  int32_t* __restrict__ status,
