@@ -10,9 +10,11 @@ HBM. The timed steps are one CUDA-graph replay of the K-step chain.
 
 Reported: value = algorithmic HBM bytes per step / time per step (GB/s, all ranks), the sweep
 kernel's roofline (a timed loop of back-to-back sweeps), the same for the FP8 E4M3 head, batched
-drafting (B = 2, 4, 8, 16 sequences per step: full head and sweep alone, BF16 and FP8), an
-end-to-end figure through the host-buffer C entry point (host->device inputs and the draft back
-each step), SM clocks sampled during the timed loops, and the CPU oracle on a bounded sample.
+drafting (B = 2, 4, 8, 16 sequences per step: full head and sweep alone, BF16 and FP8), context
+rows (R = 17 .. 4096 rows through the input stage at once), the FP8 quantiser (once per weight
+load), an end-to-end figure through the host-buffer C entry point (host->device inputs and the
+draft back each step), SM clocks sampled during the timed loops, and the CPU oracle on a bounded
+sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -345,8 +347,25 @@ def run_ours(args, world, rank, local):
             ctx_fn(max(W, 3))(stream)
         torch.cuda.synchronize()
         cgraphs[r] = capture(ctx_fn(Kb))
+    # the FP8 quantiser (offline, once per weight load), into scratch buffers: Kq calls per graph
+    Kq = 3
+    q_s = torch.empty((V, H), dtype=torch.uint8, device=dev)
+    s_s = torch.empty(V, dtype=torch.float32, device=dev)
+    graph_buffers += [q_s, s_s]
+
+    def quant_fn(n):
+        def fn(st):
+            for _ in range(n):
+                m.mtp_head_quantize_fp8(head.lm_head, q_s, s_s, status, st)
+        return fn
+
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        quant_fn(2)(stream)
     torch.cuda.synchronize()
-    for g in list(bgraphs.values()) + list(cgraphs.values()):
+    qgraph = capture(quant_fn(Kq))
+    torch.cuda.synchronize()
+    for g in list(bgraphs.values()) + list(cgraphs.values()) + [qgraph]:
         g.replay()
     torch.cuda.synchronize()
 
@@ -368,6 +387,10 @@ def run_ours(args, world, rank, local):
             results[("context", r)] = timed_graph(g, torch.cuda.current_stream())
             barrier(world)
             launches_all += 2 * Kb
+        barrier(world)
+        results["quantize"] = timed_graph(qgraph, torch.cuda.current_stream())
+        barrier(world)
+        launches_all += Kq
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}: {m.strerror(int(status.item()))}")
     drafts = tok[1:K + 1].view(-1)
@@ -428,6 +451,13 @@ def run_ours(args, world, rank, local):
         context[f"R={r}"] = {"us": round(us, 2), "rows_per_s": round(r * world / (us * 1e-6), 1),
                              "tflops": round(flops / (us * 1e-6) / 1e12, 1),
                              "frac": round(flops / (us * 1e-6) / 1e12 / tc_peak, 4)}
+    q_us = max_over_ranks(results["quantize"] / Kq, world) * 1e3
+    q_bytes = V * H * 2 + V * H + V * 4  # read the BF16 head, write codes and scales
+    quantize = {"us": round(q_us, 1), "gbs": round(q_bytes / (q_us * 1e-6) / 1e9, 1),
+                "frac": round(q_bytes / (q_us * 1e-6) / 1e9 / peak, 4), "bytes": q_bytes, "calls": Kq,
+                "timing": "Kq calls in one CUDA graph (each reads the 1.9 GB head, above L2); frac of the "
+                          "measured copy peak",
+                "kernel": "quantize_vec_kernel (offline: once per weight load)"}
     kname = "sweep_regx_kernel<BF16,H=6144,B=1>"
     achieved = sweep_bytes(2) / (results[("sweep", False)] / K * 1e-3) / 1e9
     line = {
@@ -469,6 +499,7 @@ def run_ours(args, world, rank, local):
                         kernels="row-parallel concat + tcgen05 GEMM x = concat . eh_proj^T (FP32 accumulator)",
                         timing="Kb calls in one CUDA graph; TFLOP/s of the GEMM (2 R H 2H) over the time of both "
                                "kernels; frac of the measured bf16 burst peak"),
+        "quantize_fp8": quantize,
         "gpu_launches": 2 * K,  # the BF16 chain region `value` is timed on: 2 kernels per step
         "gpu_launches_all_timed_regions": launches_all,
         "clocks": clocks.summary(),
