@@ -326,6 +326,36 @@ def test_quantizer_exhaustive_patterns_bitexact():
         assert np.array_equal(q.cpu().numpy(), qr)
 
 
+@pytest.mark.parametrize("H", [16400, 12288, 12304])
+def test_quantizer_row_widths_bitexact(H):
+    """Rows up to 24 KB are staged in shared memory, wider ones (H = 16400, 12304) stream through
+    registers: codes and scales must match the oracle bit for bit either way, including rows
+    that hold every finite pattern below their maximum and a row with a non-finite value."""
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = pats[(pats & 0x7F80) != 0x7F80]
+    rng = np.random.default_rng(H)
+    rows = []
+    for top in (0x3F80, 0x0080, 0x4300, 0x7F7F, 0x0000):
+        r = rng.permutation(finite[(finite & 0x7FFF) <= top])
+        r = np.resize(r, H)
+        r[H // 2] = top
+        rows.append(r)
+    bad = np.resize(rng.permutation(finite), H)
+    bad[H - 1] = 0x7FC0  # NaN in the last element of the row
+    rows.append(bad)
+    Wb = np.stack(rows).astype(np.uint16)
+    q_ref, s_ref, st_ref = oracle.quantize(Wb)
+    Wt = torch.from_numpy(Wb.view(np.int16)).view(torch.bfloat16).to(DEV)
+    q = torch.empty((Wb.shape[0], H), dtype=torch.uint8, device=DEV)
+    s = torch.empty(Wb.shape[0], dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.mtp_head_quantize_fp8(Wt, q, s, st)
+    torch.cuda.synchronize()
+    assert st_ref == m.ERR_NONFINITE and int(st.item()) == m.ERR_NONFINITE
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
 def test_quantizer_rejects_nonfinite_rows():
     W = torch.randn((6, 64)) * 0.02
     W[2, 5] = float("nan")
