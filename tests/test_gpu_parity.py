@@ -328,9 +328,9 @@ def test_quantizer_exhaustive_patterns_bitexact():
 
 @pytest.mark.parametrize("H", [16400, 12288, 12304])
 def test_quantizer_row_widths_bitexact(H):
-    """Rows up to 24 KB are staged in shared memory, wider ones (H = 16400, 12304) stream through
-    registers: codes and scales must match the oracle bit for bit either way, including rows
-    that hold every finite pattern below their maximum and a row with a non-finite value."""
+    """Wide rows: the load batches of both passes end ragged for H = 16400 and 12304 and exactly
+    for 12288. Codes and scales must match the oracle bit for bit, for rows that hold every
+    finite pattern below their maximum and for a row whose last element is a NaN."""
     pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     finite = pats[(pats & 0x7F80) != 0x7F80]
     rng = np.random.default_rng(H)
