@@ -299,6 +299,58 @@ def test_workspace_reused_across_batch_sizes():
         check_logits_and_draft(lg.cpu().numpy(), dr.cpu().numpy(), ref[:B], TOL_BF16)
 
 
+@pytest.mark.parametrize("B", [1, 3])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_output_stage_at_the_largest_hidden_size(B, fp8):
+    """H = 65536, the largest the entry points take: the single-sequence stage holds xhat in
+    128 KB of shared memory (plain kernel), the batched one builds it per stage (tensor-core
+    kernel). V = 1031 ends in a ragged row tile."""
+    H, V = 65536, 1031
+    g = torch.Generator().manual_seed(65536 + B)
+    W = (torch.randn((V, H), generator=g) * 0.02).to(torch.bfloat16)
+    wf = (1.0 + 0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    x = torch.randn((B, H), generator=g).to(torch.bfloat16)
+    Wd, wfd, xd = W.to(DEV), wf.to(DEV), x.to(DEV)
+    if fp8:
+        q = torch.empty((V, H), dtype=torch.uint8, device=DEV)
+        sc = torch.empty(V, dtype=torch.float32, device=DEV)
+        qst = torch.zeros(1, dtype=torch.int32, device=DEV)
+        m.mtp_head_quantize_fp8(Wd, q, sc, qst)
+        torch.cuda.synchronize()
+        q_ref, s_ref, _ = oracle.quantize(_bits(W))
+        assert int(qst.item()) == 0 and np.array_equal(_bits(q), q_ref)
+        Wg, scale, wt, tol, Wb, sb = q, sc, m.W_FP8_E4M3, TOL_FP8, q_ref, s_ref
+    else:
+        Wg, scale, wt, tol, Wb, sb = Wd, None, m.W_BF16, TOL_BF16, _bits(W), None
+    xhat = oracle.final_norm(_bits(x), _bits(wf), EPS)
+    ref = oracle.logits(wt, Wb, sb, xhat, threads=8).reshape(B, V)
+    logits = torch.full((B, V), float("nan"), dtype=torch.float32, device=DEV)
+    draft = torch.empty(B, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.mtp_head_logits_argmax_batched(xd, wfd, Wg, scale, wt, logits, draft, m.workspace(B, H, V, DEV), st, EPS)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    err = check_logits_and_draft(logits.cpu().numpy(), draft.cpu().numpy(), ref, tol)
+    assert err < 5e-3
+
+
+def test_output_stage_without_a_kernel_for_the_shape():
+    """Odd H near the maximum with B >= 2: xhat of two sequences does not fit in shared memory
+    and the tensor-core kernel needs H % 8 == 0, so the call returns MTP_ERR_NOT_IMPLEMENTED
+    before launching anything, and the outputs stay untouched."""
+    H, V, B = 65535, 64, 2
+    W = torch.zeros((V, H), dtype=torch.bfloat16, device=DEV)
+    wf = torch.ones(H, dtype=torch.bfloat16, device=DEV)
+    x = torch.ones((B, H), dtype=torch.bfloat16, device=DEV)
+    logits = torch.full((B, V), 3.0, dtype=torch.float32, device=DEV)
+    draft = torch.full((B,), -5, dtype=torch.int32, device=DEV)
+    with pytest.raises(m.MTPError) as e:
+        m.mtp_head_logits_argmax_batched(x, wf, W, None, m.W_BF16, logits, draft, m.workspace(B, H, V, DEV), None, EPS)
+    assert e.value.code == m.ERR_NOT_IMPLEMENTED
+    torch.cuda.synchronize()
+    assert bool((logits == 3.0).all()) and bool((draft == -5).all())
+
+
 def test_quantizer_exhaustive_patterns_bitexact():
     pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     finite = pats[(pats & 0x7F80) != 0x7F80]
