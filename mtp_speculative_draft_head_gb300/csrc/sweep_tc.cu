@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   // f16 of xhat * 2^k (exact inside the f16 range)
                   const float xs = nrm[2 * kSeq + n];
                   auto f16x2 = [xs](uint32_t v) {
-                    return f16_bits(__fmul_rn(bf16_lo(v), xs)) | (f16_bits(__fmul_rn(bf16_hi(v), xs)) << 16);
+                    return f16x2_bits(__fmul_rn(bf16_lo(v), xs), __fmul_rn(bf16_hi(v), xs));
                   };
                   o = make_uint4(f16x2(o.x), f16x2(o.y), f16x2(o.z), f16x2(o.w));
                 }

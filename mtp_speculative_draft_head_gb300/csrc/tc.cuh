@@ -43,10 +43,12 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
       : "=r"(lo), "=r"(hi)
       : "r"(w));
 }
-__device__ __forceinline__ uint32_t f16_bits(float v) {
-  unsigned short h;
-  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(v));
-  return h;
+// f16 bits of two values, round to nearest: lo in bits 0..15, hi in bits 16..31 (one paired
+// conversion: at B = 16 the FP8 sweep's builders spent ~17 us of it on single conversions)
+__device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
 }
 // BF16 bits of v, round to nearest even (NaN stays NaN)
 __device__ __forceinline__ uint32_t bf16_bits_rn(float v) {
