@@ -18,8 +18,10 @@
  *
  * Conventions for every entry point
  *   - Pointers are DEVICE pointers unless the argument says "host". The caller owns every
- *     buffer (weights, activations, outputs, workspace); the library allocates nothing and
- *     keeps no state beyond cached device attributes.
+ *     buffer (weights, activations, outputs, workspace). The library allocates nothing and
+ *     keeps no state beyond cached device attributes, with two stated exceptions: the pinned
+ *     staging buffers and recorded graphs of mtp_head_forward_host, and the fixed workspace
+ *     array of mtp_head_logits_argmax_batched_noalloc.
  *   - BF16 values are passed as uint16_t bit patterns, FP8 E4M3 codes as uint8_t (OCP E4M3
  *     "fn": bias 7, subnormals, max 448, no infinities). All matrices are row-major and dense.
  *   - Base pointers of matrices and vectors must be 16-byte aligned (every cudaMalloc /
