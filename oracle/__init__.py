@@ -69,6 +69,12 @@ def _load():
         lib.mo_quantize_row.restype = ctypes.c_int
         lib.mo_quantize.argtypes = [P, I64, I64, P, P]
         lib.mo_quantize.restype = ctypes.c_int
+        lib.mo_pick_combine.argtypes = [P, P, I64]
+        lib.mo_pick_combine.restype = I64
+        lib.mo_xchg_pack.argtypes = [ctypes.c_int, ctypes.c_uint16, I64, P]
+        lib.mo_xchg_sum.argtypes = [P, P, P]
+        lib.mo_xchg_pick.argtypes = [P]
+        lib.mo_xchg_pick.restype = I64
         _lib = lib
         return lib
 
@@ -217,6 +223,44 @@ def argmax(values) -> int:
     """Lowest index among equal maxima; NaN never wins; -1 if all are NaN."""
     a = _c(np.asarray(values, np.float64), np.float64)
     return int(_load().mo_argmax(_p(a), a.size))
+
+
+def shard_pick(logits, v0: int, n: int) -> tuple[float, int]:
+    """A vocabulary shard's offer: (value, global index) of the lowest-index maximum of the
+    logits of rows [v0, v0 + n), or (nan, -1) when there is none."""
+    seg = np.asarray(logits, np.float64)[v0:v0 + n]
+    i = argmax(seg)
+    return (float("nan"), -1) if i < 0 else (float(seg[i]), v0 + i)
+
+
+def pick_combine(values, indices) -> int:
+    """The draft from R shards' offers (value, global index): largest value, lowest index."""
+    v = _c(np.asarray(values, np.float64), np.float64)
+    i = _c(np.asarray(indices, np.int64), np.int64)
+    assert v.shape == i.shape
+    return int(_load().mo_pick_combine(_p(v), _p(i), v.size))
+
+
+def xchg_pack(rank: int, value_bf16: int, global_index: int) -> np.ndarray:
+    """The source's eight BF16 exchange lanes as rank ``rank`` (0 or 1) writes them."""
+    lanes = np.zeros(8, np.uint16)
+    _load().mo_xchg_pack(int(rank), int(value_bf16), int(global_index), _p(lanes))
+    return lanes
+
+
+def xchg_sum(a, b) -> np.ndarray:
+    """The SUM all-reduce of two ranks' lanes (BF16 element sums)."""
+    a = _c(np.asarray(a, np.uint16), np.uint16)
+    b = _c(np.asarray(b, np.uint16), np.uint16)
+    out = np.zeros(8, np.uint16)
+    _load().mo_xchg_sum(_p(a), _p(b), _p(out))
+    return out
+
+
+def xchg_pick(lanes) -> int:
+    """The global index the source's exchange decides for (`>=`: rank 0 wins a tie)."""
+    lanes = _c(np.asarray(lanes, np.uint16), np.uint16)
+    return int(_load().mo_xchg_pick(_p(lanes)))
 
 
 def quantize(W):

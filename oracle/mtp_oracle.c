@@ -232,6 +232,60 @@ int64_t mo_argmax(const double* v, int64_t n) {
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* The pick over vocabulary shards ([mtp] the vocab-shard fields `head_rank`, `head_v0`, */
+/* `head_n` and `forward_one`'s sharded branch: each rank sweeps its own row range and   */
+/* the ranks' (max logit, global index) pairs decide the draft; `>=` lets the lower     */
+/* rank, i.e. the lower row range, win a tie). Shard r offers (value[r], index[r]), its */
+/* own lowest-index maximum as a global row index, or index < 0 when it has none (no    */
+/* rows, or all NaN). Returns the index of the largest value, the lowest index among    */
+/* equal values, or -1 when no shard offers anything. NaN never wins.                   */
+/* ------------------------------------------------------------------------------------ */
+int64_t mo_pick_combine(const double* value, const int64_t* index, int64_t R) {
+    int64_t best = -1;
+    double best_v = 0.0;
+    for (int64_t r = 0; r < R; ++r) {
+        if (index[r] < 0 || isnan(value[r])) continue;
+        if (best < 0 || value[r] > best_v || (value[r] == best_v && index[r] < best)) {
+            best = index[r];
+            best_v = value[r];
+        }
+    }
+    return best;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* The source's own two-rank exchange ([mtp] `forward_one`, sharded branch, and the      */
+/* `head_xchg` field of the proposer state): eight BF16 lanes,                           */
+/*   lane 0, 1          the max logit of rank 0, rank 1 (BF16, as the source's logits)   */
+/*   lane 2 + 3r + d    digit d (d = 0, 1, 2; base 256, least significant first) of rank */
+/*                      r's global index, as a BF16 number                               */
+/* Each rank writes only its own lanes and leaves the rest zero; a SUM all-reduce over   */
+/* BF16 elements then hands every rank both ranks' lanes unchanged (adding zero is       */
+/* exact), and BF16 holds the integers 0..256 exactly, hence the base-256 digits. The    */
+/* winner is rank 0 when lane 0 >= lane 1, else rank 1, and its digits give the index.   */
+/* ------------------------------------------------------------------------------------ */
+void mo_xchg_pack(int rank, uint16_t value_bf16, int64_t global_index, uint16_t* lanes) {
+    for (int i = 0; i < 8; ++i) lanes[i] = 0;
+    lanes[rank] = value_bf16;
+    for (int d = 0; d < 3; ++d) {
+        double digit = (double)((global_index >> (8 * d)) & 0xFF);
+        lanes[2 + rank * 3 + d] = mo_f64_to_bf16(digit);
+    }
+}
+
+/* The SUM all-reduce of two ranks' lanes: each lane is the BF16 rounding of the sum. */
+void mo_xchg_sum(const uint16_t* a, const uint16_t* b, uint16_t* out) {
+    for (int i = 0; i < 8; ++i) out[i] = mo_f64_to_bf16(mo_bf16_to_f64(a[i]) + mo_bf16_to_f64(b[i]));
+}
+
+int64_t mo_xchg_pick(const uint16_t* lanes) {
+    int win = (mo_bf16_to_f64(lanes[0]) >= mo_bf16_to_f64(lanes[1])) ? 0 : 1;
+    int64_t index = 0;
+    for (int d = 0; d < 3; ++d) index += (int64_t)mo_bf16_to_f64(lanes[2 + win * 3 + d]) << (8 * d);
+    return index;
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* FP8 quantiser for one row ([mtp] `head_fp8` doc: the E4M3 copy of lm_head).          */
 /*   s = fp32(absmax_k |w_k| / 448);  q_k = e4m3_rne_satfinite( fp32(w_k / s) )          */
 /* A zero row gives s = 0 and zero codes. Returns MO_ERR_NONFINITE if any weight is NaN  */

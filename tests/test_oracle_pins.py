@@ -433,3 +433,102 @@ def test_planted_ties_lowest_index_wins():
     lg8 = oracle.logits(1, q, s, xh)
     assert lg8[40] == lg8[512] == lg8[911] == lg8.max()
     assert oracle.argmax(lg8) == 40
+
+
+# ---------------------------------------------------------------------- vocabulary shards
+def _bf16_logits(rng, V, levels=7):
+    """BF16-valued logits with many exact ties (a few levels), as fp64."""
+    vals = rng.integers(-levels, levels + 1, V).astype(np.float64) * 0.125
+    return oracle.bf16_to_f64(oracle.f64_to_bf16(vals))
+
+
+def _edges(rng, V, R):
+    """R contiguous ranges covering [0, V): random, possibly empty, cut points."""
+    cuts = np.sort(rng.integers(0, V + 1, R - 1))
+    return np.concatenate([[0], cuts, [V]]).astype(np.int64)
+
+
+def test_pick_combine_brute_force_equals_full_argmax():
+    """The pick over any split into shards, each offering its own lowest-index maximum, is the
+    lowest-index maximum of the whole vocabulary (ties across a boundary go to the lower range,
+    the `>=` rule of the source's cross-rank pick); NaN and -inf included."""
+    rng = np.random.default_rng(11)
+    for trial in range(400):
+        V = int(rng.integers(1, 60))
+        lg = _bf16_logits(rng, V, levels=int(rng.integers(0, 4)))
+        specials = rng.random(V)
+        lg[specials < 0.1] = np.nan
+        lg[(specials >= 0.1) & (specials < 0.15)] = -np.inf
+        lg[(specials >= 0.15) & (specials < 0.17)] = np.inf
+        R = int(rng.integers(1, 9))
+        e = _edges(rng, V, R)
+        offers = [oracle.shard_pick(lg, int(e[r]), int(e[r + 1] - e[r])) for r in range(R)]
+        got = oracle.pick_combine([o[0] for o in offers], [o[1] for o in offers])
+        assert got == oracle.argmax(lg), (trial, lg, e)
+
+
+def test_pick_combine_special_cases():
+    nan = float("nan")
+    assert oracle.pick_combine([], []) == -1
+    assert oracle.pick_combine([nan, nan], [-1, -1]) == -1
+    assert oracle.pick_combine([nan, 1.0], [3, 7]) == 7          # NaN never wins
+    assert oracle.pick_combine([2.0, 2.0], [9, 4]) == 4          # tie: lowest index
+    assert oracle.pick_combine([-0.0, 0.0], [5, 2]) == 2         # -0 == +0
+    assert oracle.pick_combine([-np.inf, -5.0], [0, 8]) == 8
+    assert oracle.pick_combine([-np.inf], [3]) == 3              # -inf wins when alone
+
+
+def test_xchg_lanes_adding_zero_is_exact():
+    """The source's SUM all-reduce hands each rank the other's lanes unchanged because adding
+    zero is exact: every non-NaN BF16 pattern plus +0 is itself (-0 + +0 gives +0, equal)."""
+    pats = np.arange(65536, dtype=np.uint16)
+    keep = ~np.isnan(oracle.bf16_to_f64(pats))
+    zero = np.zeros(8, np.uint16)
+    for p in pats[keep][::37]:
+        lanes = np.full(8, p, np.uint16)
+        out = oracle.xchg_sum(lanes, zero)
+        want = 0 if p == 0x8000 else p
+        assert np.all(out == want)
+
+
+def test_xchg_lanes_digits_are_exact_only_through_256():
+    """BF16 holds the integers 0..256 exactly (eight significant bits), so base-256 digits
+    survive the exchange; 257 does not, which is why a token id travels as digits."""
+    ints = np.arange(0, 300, dtype=np.float64)
+    back = oracle.bf16_to_f64(oracle.f64_to_bf16(ints))
+    assert np.array_equal(back[:257], ints[:257])
+    assert back[257] != 257.0
+    for g in (0, 255, 256, 65535, 65536, 154879, 2 ** 24 - 1):
+        lanes = oracle.xchg_pack(1, 0x3F80, g)  # rank 1, value 1.0
+        assert oracle.xchg_pick(oracle.xchg_sum(oracle.xchg_pack(0, 0xBF80, 0), lanes)) == g
+
+
+def test_xchg_lanes_two_ranks_brute_force():
+    """With BF16 logits (the source's logit type) the source's two-rank exchange of each
+    half's maximum gives the lowest-index maximum of the whole vocabulary: a tie across the
+    halves goes to rank 0, the lower range."""
+    rng = np.random.default_rng(5)
+    for trial in range(300):
+        V = 2 * int(rng.integers(1, 40))
+        if trial % 50 == 0:
+            V = 2 * 100000  # indices beyond 2^16 use the third digit
+        lg = _bf16_logits(rng, V, levels=int(rng.integers(0, 3)))
+        n = V // 2
+        lanes = np.zeros(8, np.uint16)
+        for rank in (0, 1):
+            v, g = oracle.shard_pick(lg, rank * n, n)
+            lanes = oracle.xchg_sum(lanes, oracle.xchg_pack(rank, int(oracle.f64_to_bf16(np.array([v]))[0]), g))
+        assert oracle.xchg_pick(lanes) == oracle.argmax(lg), trial
+
+
+def test_xchg_lanes_round_fp32_maxima_that_the_exact_pick_separates():
+    """Reading of the pages: the BF16 value lanes fit the source's BF16 logits. With FP32
+    logits two close maxima can round to one BF16 value; the lanes then give rank 0 although
+    rank 1 holds the larger logit, while the exact pick does not lose the difference."""
+    v0, v1 = 1.0, 1.0 + 2.0 ** -12          # distinct in FP32, equal after BF16 rounding
+    b0 = int(oracle.f64_to_bf16(np.array([v0]))[0])
+    b1 = int(oracle.f64_to_bf16(np.array([v1]))[0])
+    assert b0 == b1
+    lanes = oracle.xchg_sum(oracle.xchg_pack(0, b0, 10), oracle.xchg_pack(1, b1, 20))
+    assert oracle.xchg_pick(lanes) == 10
+    assert oracle.pick_combine([v0, v1], [10, 20]) == 20
