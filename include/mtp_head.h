@@ -162,6 +162,53 @@ int mtp_head_logits_argmax(const uint16_t* x, const uint16_t* final_norm_w, cons
                            int V, float eps, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Output stage over one vocabulary shard ("glm5next_mtp_head.rs": the vocab-shard geometry
+ * `head_rank` / `head_v0` / `head_n` -- a rank sweeps rows [head_v0, head_v0 + head_n) of the
+ * shared lm_head, and its FP8 copy covers that shard only -- and `forward_one`'s sharded branch
+ * with its cross-rank pick). The same kernels as mtp_head_logits_argmax_batched, over the n rows
+ * that start at global row v0:
+ *
+ *   lm_head_shard    [n, H]  BF16 or E4M3 codes: the shard's rows (row v0 of the full matrix;
+ *                            16-byte aligned, as for the output stage)
+ *   row_scale_shard  [n]     fp32 scales of those rows (FP8), NULL for BF16
+ *   v0, n                    the shard's first global row and its row count; 0 <= v0,
+ *                            1 <= n, v0 + n <= 2^31 - 1 (else MTP_ERR_SHAPE)
+ *   logits           [B, n]  fp32, optional: the shard's logits (column j is global row v0 + j)
+ *   pick             [B]     int64 output, 8-byte aligned: each sequence's exchange key of its
+ *                            (max logit, lowest global index) over the shard -- see below
+ *   draft            [B]     int32, optional: the shard's own draft as a global index
+ *   x, final_norm_w, status, workspace, B, H, eps, stream   as for the output stage
+ *
+ * Exchange key. One int64 per sequence whose signed order is the argmax order: the larger FP32
+ * value first, then the lower global index (-0 counts as +0). The pick over any set of shards is
+ * therefore the plain maximum of their keys -- mtp_head_pick_combine on one GPU, or a MAX
+ * all-reduce of the [B] keys between ranks -- exact and for any number of shards. The source
+ * exchanges BF16 lanes (each rank's max logit and three base-256 digits of its index) through a
+ * SUM all-reduce, because its all-reduce sums BF16 elements; with FP32 logits a BF16 lane would
+ * round two close maxima to one value, so the key carries the FP32 value whole. A shard whose
+ * logits are all NaN gives the empty key INT64_MIN, below every other key.
+ * ---------------------------------------------------------------------------------------- */
+int mtp_head_logits_argmax_shard(const uint16_t* x, const uint16_t* final_norm_w,
+                                 const void* lm_head_shard, const float* row_scale_shard,
+                                 int w_dtype, int v0, int n, float* logits, int64_t* pick,
+                                 int32_t* draft, int32_t* status, void* workspace,
+                                 size_t workspace_bytes, int B, int H, float eps, void* stream);
+
+/* The pick over R shards: picks [R, B] int64 (row r = shard r's keys, 8-byte aligned) ->
+ * draft [B] int32 (the global index of the largest key; -1 when every key of that sequence is
+ * empty) and value [B] fp32 (optional, may be NULL: the winning logit). One small kernel on
+ * `stream`; 1 <= R <= 65536, 1 <= B <= 16. After a MAX all-reduce between ranks, R = 1 decodes. */
+int mtp_head_pick_combine(const int64_t* picks, int R, int B, int32_t* draft, float* value,
+                          void* stream);
+
+/* The exchange key on the host (no GPU involved): the key of (value, global index), and its
+ * index and value back. mtp_head_pick_key returns INT64_MIN for index < 0 or a NaN value;
+ * mtp_head_pick_index returns -1 and mtp_head_pick_value NaN for that key. */
+int64_t mtp_head_pick_key(float value, int32_t index);
+int32_t mtp_head_pick_index(int64_t key);
+float mtp_head_pick_value(int64_t key);
+
+/* ------------------------------------------------------------------------------------------
  * Output stage without a caller-provided workspace. The source pages have no counterpart: this
  * entry point exists for callers of this library that cannot allocate device memory -- e.g. a
  * plug-in that only receives the buffers its host framework hands it and has no allocator of
@@ -172,11 +219,16 @@ int mtp_head_logits_argmax(const uint16_t* x, const uint16_t* final_norm_w, cons
  * every GPU that loads the library holds it until the process exits. B outside 1..16 returns
  * MTP_ERR_SHAPE before anything runs.
  *   - The first call on a device looks up that array's device address (once per device, with
- *     the device current). Make that first call before any stream capture on the device.
+ *     the device current). Make that first call before any stream capture on the device. The
+ *     address is kept for the life of the process: after cudaDeviceReset (or any reset of the
+ *     device's primary context) the library's device array is a new one and the kept address is
+ *     stale, so do not call this entry point on a device after resetting it.
  *   - All calls share the one array. The call clears its counter on `stream` before launching,
  *     so it never depends on what a previous call left there, but calls that may run at the
  *     same time on the GPU (different streams, or different host threads) race on it: order
- *     them on one stream or use mtp_head_logits_argmax_batched with separate workspaces.
+ *     them on one stream or use mtp_head_logits_argmax_batched with separate workspaces. The
+ *     clearing is a memset between the preceding kernel and the sweep, so unlike the workspace
+ *     entry point the sweep cannot start its weight stream before the preceding kernel ends.
  * ---------------------------------------------------------------------------------------- */
 int mtp_head_logits_argmax_batched_noalloc(const uint16_t* x, const uint16_t* final_norm_w,
                                            const void* lm_head, const float* row_scale,
@@ -248,6 +300,23 @@ int mtp_head_forward_host(const uint16_t* embed, const uint16_t* enorm_w,
  * ---------------------------------------------------------------------------------------- */
 int mtp_head_quantize_fp8(const uint16_t* w, uint8_t* q, float* row_scale, int32_t* status,
                           int V, int H, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Give-up time of the kernels' stage waits (no counterpart on the source pages, which have no
+ * device-side waits: this library's kernels wait on shared-memory barriers for their weight
+ * copies and for each other's stages, and every such wait is bounded so that a stalled copy can
+ * never hang the GPU). Past the limit the kernel stores MTP_ERR_TIMEOUT in `status`, lets its own
+ * copies in flight land, and returns; the draft and logits of that call are then undefined, and
+ * the workspace is left ready for the next call. Default 2 s (2000000000 ns), far above any
+ * real wait. The limit applies to the output-stage kernels (every batch size) and to the
+ * single-sequence input stage, launched after this call (a CUDA graph keeps the limit it was
+ * recorded with); the batched input stage and the context-row kernels always use 2 s, and so
+ * does every wait for a kernel's own copies before it exits. Process-wide; returns the previous
+ * limit. A short limit (a few ns: the device clock it is compared with advances about once a
+ * microsecond) makes the waits that find their data missing run out; ns = 0 makes every stage
+ * wait give up at once, whatever the data. Both put the error path within reach of a test.
+ * ---------------------------------------------------------------------------------------- */
+unsigned long long mtp_head_set_wait_limit_ns(unsigned long long ns);
 
 /* Static description of a status code (never NULL). */
 const char* mtp_head_strerror(int status);

@@ -44,6 +44,12 @@ SIGNATURES = {
     "mtp_head_quantize_fp8": (I, [P, P, P, P, I, I, P]),
     "mtp_head_context_rows": (I, [P, P, P, P, P, P, P, P, P, Z, I, I, I, F, P]),
     "mtp_head_context_workspace_bytes": (Z, [I, I]),
+    "mtp_head_logits_argmax_shard": (I, [P, P, P, P, I, I, I, P, P, P, P, P, Z, I, I, F, P]),
+    "mtp_head_pick_combine": (I, [P, I, I, P, P, P]),
+    "mtp_head_pick_key": (ctypes.c_int64, [F, ctypes.c_int32]),
+    "mtp_head_pick_index": (ctypes.c_int32, [ctypes.c_int64]),
+    "mtp_head_pick_value": (F, [ctypes.c_int64]),
+    "mtp_head_set_wait_limit_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
     "mtp_head_strerror": (ctypes.c_char_p, [I]),
 }
 
@@ -74,6 +80,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         if path is None:
             _lib = lib
         return lib
+
+
+def mtp_head_set_wait_limit_ns(ns: int) -> int:
+    """Give-up time (ns) of the kernels' stage waits for later launches; returns the previous
+    one. ns = 0: every stage wait gives up at once (the error path on demand)."""
+    return int(load().mtp_head_set_wait_limit_ns(int(ns)))
 
 
 def strerror(code: int) -> str:
@@ -200,6 +212,43 @@ def mtp_head_logits_argmax_batched_noalloc(x, final_norm_w, lm_head, row_scale, 
         _dev(row_scale, "row_scale"), int(w_dtype), _dev(logits, "logits"), _dev(draft, "draft"),
         _dev(status, "status"), B, H, V, eps, _stream(stream)),
         "mtp_head_logits_argmax_batched_noalloc")
+
+
+def mtp_head_logits_argmax_shard(x, final_norm_w, lm_head_shard, row_scale_shard, w_dtype: int, v0: int,
+                                 logits, pick, draft, ws, status=None, eps: float = 1e-6, stream=None) -> None:
+    """Output stage over the vocabulary rows [v0, v0 + n) (lm_head_shard holds those n rows):
+    pick [B] int64 receives each sequence's exchange key; logits [B, n] and draft [B] (a global
+    index) are optional."""
+    n, H = lm_head_shard.shape
+    B = pick.numel()
+    _check(load().mtp_head_logits_argmax_shard(
+        _dev(x, "x"), _dev(final_norm_w, "final_norm_w"), _dev(lm_head_shard, "lm_head_shard"),
+        _dev(row_scale_shard, "row_scale_shard"), int(w_dtype), int(v0), n, _dev(logits, "logits"),
+        _dev(pick, "pick"), _dev(draft, "draft"), _dev(status, "status"), _dev(ws, "workspace"),
+        ws.numel() * ws.element_size(), B, H, eps, _stream(stream)),
+        "mtp_head_logits_argmax_shard")
+
+
+def mtp_head_pick_combine(picks, draft, value=None, stream=None) -> None:
+    """draft [B] (and value [B]) from the exchange keys picks [R, B] of R vocabulary shards."""
+    B = draft.numel()
+    R = picks.numel() // B
+    _check(load().mtp_head_pick_combine(_dev(picks, "picks"), R, B, _dev(draft, "draft"), _dev(value, "value"),
+                                        _stream(stream)),
+           "mtp_head_pick_combine")
+
+
+def mtp_head_pick_key(value: float, index: int) -> int:
+    """The exchange key of (value, global index), computed on the host."""
+    return int(load().mtp_head_pick_key(float(value), int(index)))
+
+
+def mtp_head_pick_index(key: int) -> int:
+    return int(load().mtp_head_pick_index(int(key)))
+
+
+def mtp_head_pick_value(key: int) -> float:
+    return float(load().mtp_head_pick_value(int(key)))
 
 
 def mtp_head_forward_batched(embed, enorm_w, hnorm_w, eh_proj, final_norm_w, lm_head, row_scale,

@@ -18,6 +18,7 @@ namespace {
 
 using mtp::kMaxB;
 constexpr int kMaxContextRows = 65536;
+constexpr int kMaxPickShards = 65536;  // picks combined by one mtp_head_pick_combine call
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -53,15 +54,15 @@ int validate_input(const uint16_t* embed, const uint16_t* enorm_w, const uint16_
 int validate_output(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_head,
                     const float* row_scale, int w_dtype, const float* logits, const int32_t* draft,
                     const int32_t* status, const void* workspace, size_t workspace_bytes, int B,
-                    int H, int V, float eps) {
-  if (!x || !final_norm_w || !lm_head || !draft) return MTP_ERR_ARG;
+                    int H, int V, float eps, bool draft_optional = false) {
+  if (!x || !final_norm_w || !lm_head || (!draft && !draft_optional)) return MTP_ERR_ARG;
   if (w_dtype != MTP_W_BF16 && w_dtype != MTP_W_FP8_E4M3) return MTP_ERR_ARG;
   if (w_dtype == MTP_W_FP8_E4M3 && !row_scale) return MTP_ERR_ARG;
   if (check_eps(eps) != MTP_OK) return MTP_ERR_ARG;
   if (check_shape(B, H, V) != MTP_OK) return MTP_ERR_SHAPE;
   if (!aligned(x, 16) || !aligned(final_norm_w, 16) || !aligned(lm_head, 16) ||
       (row_scale && !aligned(row_scale, 4)) || (logits && !aligned(logits, 4)) ||
-      !aligned(draft, 4) || (status && !aligned(status, 4)) || (workspace && !aligned(workspace, 16)))
+      (draft && !aligned(draft, 4)) || (status && !aligned(status, 4)) || (workspace && !aligned(workspace, 16)))
     return MTP_ERR_ALIGN;
   if (!workspace || workspace_bytes < mtp::sweep_workspace_bytes(B)) return MTP_ERR_WORKSPACE;
   return MTP_OK;
@@ -100,13 +101,18 @@ int run_input(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hn
   a.V = V;
   a.eps = eps;
   a.inv_h = 1.0 / static_cast<double>(H);
+  a.wait_ns = mtp::stage_wait_ns();
   return map_cuda(mtp::launch_input_stage(a, static_cast<cudaStream_t>(stream)));
 }
 
+// index_base / pick: a vocabulary shard's first global row and its exchange keys (may be null).
 int run_output(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_head,
                const float* row_scale, int w_dtype, float* logits, int32_t* draft, int32_t* status,
-               void* workspace, int B, int H, int V, float eps, void* stream) {
+               void* workspace, int B, int H, int V, float eps, void* stream, int32_t index_base = 0,
+               int64_t* pick = nullptr) {
   mtp::SweepArgs a{};
+  a.index_base = index_base;
+  a.pick = pick;
   a.x = x;
   a.final_norm_w = final_norm_w;
   a.W = static_cast<const uint8_t*>(lm_head);
@@ -121,6 +127,7 @@ int run_output(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_h
   a.V = V;
   a.eps = eps;
   a.inv_h = 1.0 / static_cast<double>(H);
+  a.wait_ns = mtp::stage_wait_ns();
   return map_cuda(mtp::launch_sweep(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -372,6 +379,33 @@ int mtp_head_logits_argmax(const uint16_t* x, const uint16_t* final_norm_w, cons
                                         status, workspace, workspace_bytes, 1, H, V, eps, stream);
 }
 
+int mtp_head_logits_argmax_shard(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_head_shard,
+                                 const float* row_scale_shard, int w_dtype, int v0, int n, float* logits,
+                                 int64_t* pick, int32_t* draft, int32_t* status, void* workspace,
+                                 size_t workspace_bytes, int B, int H, float eps, void* stream) {
+  if (!pick) return MTP_ERR_ARG;
+  if (v0 < 0 || n < 1 || static_cast<int64_t>(v0) + n > static_cast<int64_t>(INT32_MAX)) return MTP_ERR_SHAPE;
+  if (!aligned(pick, 8)) return MTP_ERR_ALIGN;
+  const int v = validate_output(x, final_norm_w, lm_head_shard, row_scale_shard, w_dtype, logits, draft, status,
+                                workspace, workspace_bytes, B, H, n, eps, /*draft_optional=*/true);
+  if (v != MTP_OK) return v;
+  return run_output(x, final_norm_w, lm_head_shard, row_scale_shard, w_dtype, logits, draft, status, workspace, B,
+                    H, n, eps, stream, v0, pick);
+}
+
+int mtp_head_pick_combine(const int64_t* picks, int R, int B, int32_t* draft, float* value, void* stream) {
+  if (!picks || !draft) return MTP_ERR_ARG;
+  if (R < 1 || R > kMaxPickShards || B < 1 || B > kMaxB) return MTP_ERR_SHAPE;
+  if (!aligned(picks, 8) || !aligned(draft, 4) || (value && !aligned(value, 4))) return MTP_ERR_ALIGN;
+  return map_cuda(mtp::launch_pick_combine(picks, R, B, draft, value, static_cast<cudaStream_t>(stream)));
+}
+
+int64_t mtp_head_pick_key(float value, int32_t index) { return mtp::pick_key(value, index); }
+
+int32_t mtp_head_pick_index(int64_t key) { return mtp::pick_index(key); }
+
+float mtp_head_pick_value(int64_t key) { return mtp::pick_value(key); }
+
 size_t mtp_head_workspace_bytes(int B, int H, int V) {
   if (check_shape(B, H, V) != MTP_OK) return 0;
   return step_workspace_bytes(B, H);
@@ -470,6 +504,8 @@ int mtp_head_quantize_fp8(const uint16_t* w, uint8_t* q, float* row_scale, int32
     return MTP_ERR_ALIGN;
   return map_cuda(mtp::launch_quantize(w, q, row_scale, status, V, H, static_cast<cudaStream_t>(stream)));
 }
+
+unsigned long long mtp_head_set_wait_limit_ns(unsigned long long ns) { return mtp::set_stage_wait_ns(ns); }
 
 const char* mtp_head_strerror(int status) {
   switch (status) {

@@ -13,6 +13,7 @@
 #include <stdint.h>
 
 #include "../../include/mtp_head.h"
+#include "pick.h"
 
 namespace mtp {
 
@@ -64,13 +65,18 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
-// Wait for phase `parity` of an mbarrier, giving up after kWaitLimitNs. Returns false on
-// timeout; the caller records MTP_ERR_TIMEOUT and stops.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of an mbarrier, giving up after limit_ns (kWaitLimitNs unless the
+// launch carries another limit for its stage waits). Returns false on timeout; the caller
+// records MTP_ERR_TIMEOUT and stops. A limit of 0 gives up at once without looking at the
+// barrier (the error path on demand). Waits for the kernel's own copies to land before it
+// exits always take the default limit.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
+  if (limit_ns == 0) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
   return true;
 }
@@ -296,7 +302,10 @@ __device__ __forceinline__ void arg_update(ArgBest& b, float v, int32_t i) {
 // (a single thread walking all partials waited out one L2 latency per CTA, ~30 us for 152)
 // and a shuffle tree combines them. (value, lowest index) is a total order, so the result does
 // not depend on the order. All threads of the block call it.
-__device__ __forceinline__ void combine_partials(const ArgBest* part, unsigned int ncta, int nb, int32_t* draft) {
+// A vocabulary shard's sweep numbers its rows from index_base (the shard's first global row)
+// and may also store the pick's exchange key (pick.h) in pick[b]; draft and pick may be null.
+__device__ __forceinline__ void combine_partials(const ArgBest* part, unsigned int ncta, int nb, int32_t* draft,
+                                                 int32_t index_base, int64_t* pick) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   for (int b = warp; b < nb; b += nw) {
     ArgBest c{0.0f, -1};
@@ -311,7 +320,11 @@ __device__ __forceinline__ void combine_partials(const ArgBest* part, unsigned i
       const int32_t i = __shfl_xor_sync(0xffffffffu, c.i, m);
       if (i >= 0) arg_update(c, v, i);
     }
-    if (lane == 0) draft[b] = c.i;
+    if (lane == 0) {
+      const int32_t g = c.i >= 0 ? c.i + index_base : -1;
+      if (draft != nullptr) draft[b] = g;
+      if (pick != nullptr) pick[b] = pick_key(c.v, g);
+    }
   }
 }
 

@@ -2,21 +2,30 @@
 // programmatic stream serialization.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 #include <set>
 #include <utility>
 
+#include "common.cuh"
 #include "internal.h"
 
 namespace mtp {
 
 namespace {
+std::atomic<unsigned long long> g_stage_wait_ns{kWaitLimitNs};
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceInfo g_info[kMaxDevices];
 bool g_have[kMaxDevices] = {};
 std::set<std::pair<int, const void*>> g_smem_set;  // (device, kernel) with max smem raised
 }  // namespace
+
+unsigned long long stage_wait_ns() { return g_stage_wait_ns.load(std::memory_order_relaxed); }
+
+unsigned long long set_stage_wait_ns(unsigned long long ns) {
+  return g_stage_wait_ns.exchange(ns, std::memory_order_relaxed);
+}
 
 TmapEncodeFn tensor_map_encoder() {
   static std::once_flag once;

@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(NWI * 32, 1) input_tma_kernel(const InputArgs 
   };
   for (int t = 0; t < nitems; ++t) {
     const uint32_t bar = smem_addr(&my_bars[cs]);
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar, parity))) {
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, a.wait_ns))) {
       t_fail = t;
       break;
     }

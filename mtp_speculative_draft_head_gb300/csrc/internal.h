@@ -46,6 +46,11 @@ struct DeviceInfo {
 // Cached per device; returns cudaSuccess or the error of the first query.
 cudaError_t device_info(DeviceInfo* info);
 
+// Give-up time of the stage waits of the kernels launched from now on (process-wide, 2 s by
+// default); set_stage_wait_ns returns the previous value.
+unsigned long long stage_wait_ns();
+unsigned long long set_stage_wait_ns(unsigned long long ns);
+
 // cudaLaunchKernelExC with programmatic stream serialization allowed; raises the kernel's
 // dynamic shared memory limit once per device. device_info() must have been called first.
 cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
@@ -78,6 +83,7 @@ struct InputArgs {
   uint16_t* concat_ws;
   int32_t* valid_ws;
   const uint16_t* concat;  // set by that launcher: the prebuilt concat the kernel reads
+  unsigned long long wait_ns;  // give-up time of the single-sequence kernel's stage waits
 };
 
 struct SweepArgs {
@@ -86,7 +92,7 @@ struct SweepArgs {
   const uint8_t* W;      // lm_head bytes (BF16 pairs or E4M3 codes)
   const float* scale;    // FP8 row scales or nullptr
   float* logits;         // may be nullptr
-  int32_t* draft;
+  int32_t* draft;        // may be nullptr when pick is given
   int32_t* status;
   uint8_t* ws;
   int w_dtype;
@@ -94,6 +100,11 @@ struct SweepArgs {
   float eps;
   double inv_h;  // 1 / H (fp64), for the mean of squares
   int stages;
+  // Vocabulary shard: W (and scale) start at global row index_base, V is the shard's row count;
+  // the draft is a global index, and pick (may be nullptr) receives each sequence's exchange key.
+  int32_t index_base;
+  int64_t* pick;
+  unsigned long long wait_ns;  // give-up time of the stage waits
 };
 
 struct ContextArgs {
@@ -139,6 +150,10 @@ cudaError_t launch_host_out(const int32_t* draft_src, int32_t* draft_dst, const 
                             int B, cudaStream_t stream);
 cudaError_t launch_quantize(const uint16_t* w, uint8_t* q, float* scale, int32_t* status,
                             int V, int H, cudaStream_t stream);
+// Pick over R shards' exchange keys picks[r * B + b]: draft[b] (global index, -1 if empty) and
+// optionally value[b].
+cudaError_t launch_pick_combine(const int64_t* picks, int R, int B, int32_t* draft, float* value,
+                                cudaStream_t stream);
 
 // Host-side argument check of the output stage (status code, nothing launched).
 int check_output_args(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_head,

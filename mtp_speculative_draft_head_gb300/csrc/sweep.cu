@@ -43,8 +43,8 @@ namespace {
 // best[] is uniform across the lanes of a warp.
 // ------------------------------------------------------------------------------------------
 template <int NB>
-__device__ void argmax_finish(const ArgBest* best, int nb, ArgBest* wbest, uint8_t* ws,
-                              int32_t* draft) {
+__device__ void argmax_finish(const ArgBest* best, int nb, ArgBest* wbest, const SweepArgs& a) {
+  uint8_t* ws = a.ws;
   __shared__ int is_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
@@ -70,7 +70,7 @@ __device__ void argmax_finish(const ArgBest* best, int nb, ArgBest* wbest, uint8
   __syncthreads();
   if (is_last) {
     __threadfence();
-    combine_partials(part, gridDim.x, nb, draft);
+    combine_partials(part, gridDim.x, nb, a.draft, a.index_base, a.pick);
     if (threadIdx.x == 0) {
       // every CTA has finished claiming rows: ready for the next launch
       atomicExch(reinterpret_cast<unsigned int*>(ws + kRowCounterOffset), 0u);
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(NWR * 32, 1) sweep_regx_kernel(const SweepArgs
 #pragma unroll 1
   while (consumed < n_issued) {
     const int jj = consumed & (kGroup - 1);
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&my_bars[cs]), parity))) {
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&my_bars[cs]), parity, a.wait_ns))) {
       i_fail = consumed;
       break;
     }
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(NWR * 32, 1) sweep_regx_kernel(const SweepArgs
   }
   __syncwarp();
   best = warp_arg_reduce(best);
-  argmax_finish<1>(&best, 1, wbest, a.ws, a.draft);
+  argmax_finish<1>(&best, 1, wbest, a);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) sweep_tma_kernel(const SweepArgs 
     if constexpr (WT == MTP_W_FP8_E4M3) {
       if (cc == 0) row_scale = __ldg(a.scale + row);
     }
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&my_bars[cs]), parity))) {
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&my_bars[cs]), parity, a.wait_ns))) {
       t_fail = t;
       break;
     }
@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) sweep_tma_kernel(const SweepArgs 
     }
   }
   __syncwarp();
-  argmax_finish<NB>(best, NB, wbest, a.ws, a.draft);
+  argmax_finish<NB>(best, NB, wbest, a);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(kThreads) sweep_plain_kernel(const SweepArgs a
       arg_update(best[b], acc, static_cast<int32_t>(row));
     }
   }
-  argmax_finish<kMaxB>(best, nb, wbest, a.ws, a.draft);
+  argmax_finish<kMaxB>(best, nb, wbest, a);
 }
 
 cudaError_t launch_sweep_kernel(void (*kernel)(SweepArgs), unsigned grid, unsigned threads, size_t smem,

@@ -143,7 +143,8 @@ struct BFrags<MTP_W_FP8_E4M3, NT> {
 };
 
 // CTA combine of per-warp bests (wbest[warp * kSeq + b]) and the last-CTA-done grid argmax.
-__device__ void tc_argmax_finish(int nb, const ArgBest* wbest, uint8_t* ws, int32_t* draft) {
+__device__ void tc_argmax_finish(int nb, const ArgBest* wbest, const SweepArgs& a) {
+  uint8_t* ws = a.ws;
   __shared__ int is_last;
   ArgBest* part = reinterpret_cast<ArgBest*>(ws + kWsHeader);
   unsigned int* counter = reinterpret_cast<unsigned int*>(ws);
@@ -161,7 +162,7 @@ __device__ void tc_argmax_finish(int nb, const ArgBest* wbest, uint8_t* ws, int3
   __syncthreads();
   if (is_last) {
     __threadfence();
-    combine_partials(part, gridDim.x, nb, draft);
+    combine_partials(part, gridDim.x, nb, a.draft, a.index_base, a.pick);
     if (threadIdx.x == 0) atomicExch(counter, 0u);
   }
 }
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int kp = 0; kp < KP && ok; ++kp) {
           const int nsub = KB - kp * kKS < kKS ? KB - kp * kKS : kKS;
           for (int j = 0; j < ntile; ++j) {
-            if (*reinterpret_cast<volatile int*>(&abort_flag) || !mbar_wait_bounded(smem_addr(&aempty[slot]), ep)) {
+            if (*reinterpret_cast<volatile int*>(&abort_flag) || !mbar_wait_bounded(smem_addr(&aempty[slot]), ep, a.wait_ns)) {
               ok = false;
               break;
             }
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int u = 0; u < nstages; ++u) {
         const int kp = u % KP;
         if (*reinterpret_cast<volatile int*>(&abort_flag) ||
-            !__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&bempty[slot]), ep))) {
+            !__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&bempty[slot]), ep, a.wait_ns))) {
           if (lane == 0) {
             store_status(a.status, MTP_ERR_TIMEOUT);
             atomicExch(&abort_flag, 1);
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int kp = 0; kp < KP && ok; ++kp) {
           const int nsub = KB - kp * kKS < kKS ? KB - kp * kKS : kKS;
           if (*reinterpret_cast<volatile int*>(&abort_flag) ||
-              !__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&bfull[bslot]), bp))) {
+              !__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&bfull[bslot]), bp, a.wait_ns))) {
             ok = false;
             break;
           }
@@ -415,7 +416,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int j = 0; j < kTileGroup; ++j) {
             if (j < ntile && ok) {
-              if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&afull[aslot]), ap))) {
+              if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&afull[aslot]), ap, a.wait_ns))) {
                 ok = false;
               } else {
 #pragma unroll
@@ -475,7 +476,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   __syncthreads();
   pdl_wait_prior_grid();  // the workspace may still be read by the kernel before (no-op if done)
-  tc_argmax_finish(B, wbest, a.ws, a.draft);
+  tc_argmax_finish(B, wbest, a);
 }
 
 // ---------------------------------------------------------------------------- host side

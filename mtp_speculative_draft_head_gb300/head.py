@@ -140,3 +140,88 @@ class MtpDraftHead:
                 fn(s)
         torch.cuda.current_stream().wait_stream(s)
         return g
+
+
+# ---------------------------------------------------------------------- vocabulary shards
+def shard_geometry(V: int, rank: int, world: int) -> tuple[int, int]:
+    """(v0, n): the rows [v0, v0 + n) of lm_head that rank ``rank`` of ``world`` sweeps. As in the
+    source's head ("glm5next_mtp_head.rs", `head_v0` / `head_n`): the vocabulary splits into
+    ``world`` equal ranges when it divides evenly, and otherwise every rank sweeps all of it
+    (``n == V``, no exchange needed)."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("need 0 <= rank < world")
+    if V % world != 0:
+        return 0, V
+    n = V // world
+    return rank * n, n
+
+
+def exchange_picks(picks: torch.Tensor, group=None) -> torch.Tensor:
+    """The cross-rank step of the sharded head: every rank's [B] int64 exchange keys become their
+    element-wise maximum on every rank -- one MAX all-reduce of 8 bytes per sequence (the keys'
+    order is the argmax order, so the maximum is the pick). A no-op without a process group or on
+    one rank. Runs on the process group's backend (NCCL for CUDA tensors, gloo for CPU ones)."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
+        dist.all_reduce(picks, op=dist.ReduceOp.MAX, group=group)
+    return picks
+
+
+class VocabShard:
+    """The output stage of one rank of a vocabulary-sharded head: final norm, the sweep of this
+    rank's rows of lm_head (BF16, or an FP8 copy of these rows only, as in the source's
+    `head_fp8` doc), the per-sequence exchange key, the exchange with the other ranks and the
+    decode of the winning key into the draft. On one GPU, several shards' keys can also be
+    combined directly (``mtp_head_pick_combine`` with R > 1)."""
+
+    def __init__(self, lm_head: torch.Tensor, final_norm_w: torch.Tensor, rank: int, world: int,
+                 eps: float = 1e-6, max_batch: int = 16):
+        V, H = lm_head.shape
+        self.V, self.H = V, H
+        self.rank, self.world = rank, world
+        self.v0, self.n = shard_geometry(V, rank, world)
+        self.sharded = self.n != V
+        self.lm_head = lm_head[self.v0:self.v0 + self.n]
+        self.final_norm_w = final_norm_w
+        self.eps = float(eps)
+        self.device = lm_head.device
+        self.lm_head_fp8 = None
+        self.row_scale = None
+        self.ws = _lib.workspace(max_batch, H, self.n, self.device)
+
+    def quantize_fp8(self) -> int:
+        """E4M3 copy of this shard's rows with their FP32 scales; returns the device status."""
+        q = torch.empty((self.n, self.H), dtype=torch.uint8, device=self.device)
+        s = torch.empty(self.n, dtype=torch.float32, device=self.device)
+        st = torch.zeros(1, dtype=torch.int32, device=self.device)
+        _lib.mtp_head_quantize_fp8(self.lm_head, q, s, st)
+        code = int(st.item())
+        self.lm_head_fp8, self.row_scale = (q, s) if code == 0 else (None, None)
+        return code
+
+    def picks(self, x, fp8: bool = False, pick=None, logits=None, status=None, stream=None) -> torch.Tensor:
+        """This shard's exchange keys [B] for the block outputs x [B, H] (logits [B, n] optional)."""
+        B = x.shape[0]
+        if fp8 and self.lm_head_fp8 is None:
+            raise RuntimeError("no FP8 copy: call quantize_fp8() first")
+        W, s, wt = (self.lm_head_fp8, self.row_scale, W_FP8_E4M3) if fp8 else (self.lm_head, None, W_BF16)
+        pick = torch.empty(B, dtype=torch.int64, device=self.device) if pick is None else pick
+        _lib.mtp_head_logits_argmax_shard(x, self.final_norm_w, W, s, wt, self.v0, logits, pick, None, self.ws,
+                                          status, self.eps, stream)
+        return pick
+
+    def draft(self, x, fp8: bool = False, group=None, draft=None, status=None, stream=None) -> torch.Tensor:
+        """The draft [B] (global token ids) of the whole vocabulary: this shard's keys, the MAX
+        exchange with the other ranks (when sharded), then the decode. ``stream``, if given, is a
+        torch.cuda.Stream."""
+        pick = self.picks(x, fp8=fp8, status=status, stream=stream)
+        if self.sharded:
+            # the all-reduce runs on torch's current stream: order it between the two kernels
+            if stream is not None:
+                torch.cuda.current_stream().wait_stream(stream)
+            exchange_picks(pick, group)
+            if stream is not None:
+                stream.wait_stream(torch.cuda.current_stream())
+        draft = torch.empty(x.shape[0], dtype=torch.int32, device=self.device) if draft is None else draft
+        _lib.mtp_head_pick_combine(pick, draft, stream=stream)
+        return draft

@@ -34,7 +34,9 @@ def test_header_declares_the_entry_points():
                  "mtp_head_logits_argmax_batched", "mtp_head_quantize_fp8",
                  "mtp_head_workspace_bytes", "mtp_head_forward_batched", "mtp_head_forward_host",
                  "mtp_head_context_rows", "mtp_head_context_workspace_bytes",
-                 "mtp_head_logits_argmax_batched_noalloc", "mtp_head_strerror"):
+                 "mtp_head_logits_argmax_batched_noalloc", "mtp_head_logits_argmax_shard",
+                 "mtp_head_pick_combine", "mtp_head_pick_key", "mtp_head_pick_index", "mtp_head_pick_value",
+                 "mtp_head_strerror"):
         assert name in d
 
 
@@ -194,3 +196,63 @@ def test_noalloc_output_stage_validation(lib):
     f = lib.mtp_head_logits_argmax_batched_noalloc
     assert f(A, A, A, None, m.W_BF16, None, A, None, 0, 64, 100, ctypes.c_float(1e-6), None) == m.ERR_SHAPE
     assert f(A, A, A, None, m.W_BF16, None, A, None, 17, 64, 100, ctypes.c_float(1e-6), None) == m.ERR_SHAPE
+
+
+# ---------------------------------------------------------------------- vocabulary shards
+def test_shard_entry_point_validation(lib):
+    A = 0x10000  # fake, 16-byte aligned; never dereferenced
+    eps = ctypes.c_float(1e-6)
+    ws = m.mtp_head_workspace_bytes(1, 64, 100)
+
+    def call(v0=0, n=100, pick=A, draft=None, B=1, H=64):
+        return lib.mtp_head_logits_argmax_shard(A, A, A, None, m.W_BF16, v0, n, None, pick, draft, None, A, ws, B,
+                                                H, eps, None)
+    assert call(pick=None) == m.ERR_ARG
+    assert call(v0=-1) == m.ERR_SHAPE
+    assert call(n=0) == m.ERR_SHAPE
+    assert call(v0=2 ** 31 - 100, n=100) == m.ERR_SHAPE
+    assert call(pick=A + 4) == m.ERR_ALIGN
+    assert call(B=17) == m.ERR_SHAPE
+    assert call(draft=A + 2) == m.ERR_ALIGN
+
+
+def test_pick_combine_validation(lib):
+    A = 0x10000
+    assert lib.mtp_head_pick_combine(None, 2, 1, A, None, None) == m.ERR_ARG
+    assert lib.mtp_head_pick_combine(A, 2, 1, None, None, None) == m.ERR_ARG
+    assert lib.mtp_head_pick_combine(A, 0, 1, A, None, None) == m.ERR_SHAPE
+    assert lib.mtp_head_pick_combine(A, 2, 0, A, None, None) == m.ERR_SHAPE
+    assert lib.mtp_head_pick_combine(A, 2, 17, A, None, None) == m.ERR_SHAPE
+    assert lib.mtp_head_pick_combine(A + 4, 2, 1, A, None, None) == m.ERR_ALIGN
+
+
+def test_pick_key_order_is_the_argmax_order(lib):
+    """Host side of the exchange key: for random (value, index) pairs, including ties, +-0,
+    +-inf and subnormals, key(a) > key(b) exactly when a beats b in the argmax order (larger
+    value, then lower index); the key decodes back to its index and value."""
+    import numpy as np
+    rng = np.random.default_rng(3)
+    specials = np.array([0.0, -0.0, np.inf, -np.inf, 1e-45, -1e-45, 3.4e38, -3.4e38, 1.0, -1.0], np.float32)
+    vals = np.concatenate([specials, rng.standard_normal(200).astype(np.float32),
+                           np.round(rng.standard_normal(100)).astype(np.float32)])
+    idx = rng.integers(0, 2 ** 31 - 1, vals.size)
+    idx[:20] = [0, 1, 2 ** 31 - 2, 5, 5, 7, 0, 3, 3, 9] * 2
+    keys = [m.mtp_head_pick_key(float(v), int(i)) for v, i in zip(vals, idx)]
+    for k, v, i in zip(keys, vals, idx):
+        assert m.mtp_head_pick_index(k) == int(i)
+        got = m.mtp_head_pick_value(k)
+        assert got == float(v) and (v != 0 or np.signbit(np.float32(got)) == False)  # noqa: E712
+    for a in range(0, vals.size, 3):
+        for b in range(vals.size):
+            va, vb, ia, ib = float(vals[a]), float(vals[b]), int(idx[a]), int(idx[b])
+            beats = va > vb or (va == vb and ia < ib)
+            assert (keys[a] > keys[b]) == beats, (va, ia, vb, ib)
+
+
+def test_pick_key_empty(lib):
+    empty = -2 ** 63
+    assert m.mtp_head_pick_key(float("nan"), 4) == empty
+    assert m.mtp_head_pick_key(1.0, -1) == empty
+    assert m.mtp_head_pick_index(empty) == -1
+    assert m.mtp_head_pick_value(empty) != m.mtp_head_pick_value(empty)  # NaN
+    assert m.mtp_head_pick_key(float("-inf"), 2 ** 31 - 1) > empty
