@@ -91,20 +91,43 @@ def test_glm_head(glm, B, fp8):
     assert err < 5e-3
 
 
-def test_glm_chain_1000_teacher_forced(glm):
+@pytest.mark.parametrize("fp8", [False, True])
+def test_glm_chain_1000_teacher_forced(glm, fp8):
+    """The 1000-token chain: each step feeds its draft (device-resident) into the next. The graph
+    replay and an eager run of the same 1000 steps must give the same drafts at every step; 33
+    evenly spaced steps are checked against the oracle, fed the token the GPU used (teacher
+    forcing), and on four of them the full logits of that step are compared element by element."""
     steps = 1000
     hiddens = torch.cat([synth.chain_hidden(glm.H, i + 1, DEV) for i in range(steps)]).view(steps, 1, glm.H)
     first = synth.chain_first_token(glm.V, DEV)
-    drafts = glm.head.chain(first, hiddens, graph=True).cpu().view(-1).numpy()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    drafts = glm.head.chain(first, hiddens, fp8=fp8, graph=True, status=status).cpu().view(-1).numpy()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
     assert np.all((drafts >= 0) & (drafts < glm.V))
-    eager = glm.head.chain(first, hiddens[:20], graph=False).cpu().view(-1).numpy()
-    assert np.array_equal(eager, drafts[:20])
+    eager = glm.head.chain(first, hiddens, fp8=fp8, graph=False, status=status).cpu().view(-1).numpy()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(eager, drafts), f"first differing step {int(np.nonzero(eager != drafts)[0][0])}"
     toks = np.concatenate([first.cpu().numpy(), drafts])
-    for i in (0, 499, 999):
+    checked = sorted(set(range(0, steps, 31)) | {steps - 1})
+    assert len(checked) >= 32
+    with_logits = set(checked[::len(checked) // 4][:4])
+    tol = TOL_FP8 if fp8 else TOL_BF16
+    for i in checked:
+        tok = torch.tensor([int(toks[i])], dtype=torch.int32, device=DEV)
         xr, _ = oracle.input_stage(glm.wb["embed"], glm.wb["enorm_w"], glm.wb["hnorm_w"], glm.wb["eh_proj"],
                                    [int(toks[i])], _bits(hiddens[i]), EPS)
-        ref = glm.oracle_logits(xr, False)
-        check_draft(int(drafts[i]), None, ref[0], TOL_BF16)
+        ref = glm.oracle_logits(xr, fp8)
+        if i in with_logits:
+            # the same step again with the logits stored: its draft is the chain's, bit for bit
+            x, logits, d = glm.head.forward(tok, hiddens[i], fp8=fp8, logits=True, status=status)
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0
+            assert int(d.item()) == int(drafts[i])
+            check_logits_and_draft(logits.cpu().numpy(), d.cpu().numpy(), ref, tol)
+        else:
+            check_draft(int(drafts[i]), None, ref[0], tol)
 
 
 def test_adversarial_ties_and_outliers():

@@ -4,8 +4,8 @@ mtp_head_logits_argmax_batched_noalloc is for callers of this library that canno
 device memory (a plug-in that only gets the buffers its host hands it, a process whose device
 memory another allocator has already claimed): it keeps the output stage's small workspace in
 a fixed array inside the library instead of taking one from the caller. Here it must give the
-same logits and drafts as mtp_head_logits_argmax_batched with a caller-provided workspace, on
-two calls in a row (the second call reuses the array the first one left behind).
+same logits (bit for bit) and drafts as mtp_head_logits_argmax_batched with a caller-provided
+workspace, on two calls in a row (the second call reuses the array the first one left behind).
 
 This file is collected last on purpose, and needs nothing from the other test files.
 """
@@ -66,8 +66,11 @@ def test_noalloc_matches_workspace_entry_point_twice(H, V, B, fp8):
         assert _raw_noalloc(lib, x, g["final_norm_w"], W, s, wt, logits, draft, status, B, H, V) == m.OK
         torch.cuda.synchronize()
         assert int(status.item()) == 0
+        # the same kernels on the same inputs: the logits must agree bit for bit, not only within
+        # the parity tolerance (which still bounds any difference, were there one)
         err = float((logits.double() - ref_logits.double()).abs().max())
         assert err <= tol, err
+        assert torch.equal(logits.view(torch.int32), ref_logits.view(torch.int32))
         assert torch.equal(draft, ref_draft)
         lg = logits.cpu().numpy()
         for b in range(B):  # each draft is the lowest-index argmax of its own logits
