@@ -8,15 +8,18 @@ stage (embedding gather, enorm, hnorm, concat, eh_proj) and the fused output sta
 lm_head sweep, argmax) -- 2.05 GB of weights streamed per step, 16x the L2, so every step reads
 HBM. The timed steps are one CUDA-graph replay of the K-step chain.
 
-Reported: value = algorithmic HBM bytes per step / time per step (GB/s, all ranks), the sweep
-kernel's roofline (a timed loop of back-to-back sweeps), the same for the FP8 E4M3 head, batched
-drafting (B = 2, 4, 8, 16 sequences per step: full head and sweep alone, BF16 and FP8), context
-rows (R = 17 .. 4096 rows through the input stage at once), the FP8 quantiser (once per weight
-load), an end-to-end figure through the host-buffer C entry point (host->device inputs and the
-draft back each step), SM clocks sampled during the timed loops, and the CPU oracle on a bounded
-sample.
+Reported: value = algorithmic HBM bytes per step / time per step (GB/s, all ranks); the sweep
+kernel's roofline (a timed loop of back-to-back sweeps that store their logits), the same for the
+FP8 E4M3 head (`fp8_b1`); each stage alone with and without stored logits (`stages`); the
+adversarial workload with ties and outliers, H=4096, V=131072 (`adversarial`); batched drafting
+(B = 2, 4, 8, 16 sequences per step: full head and sweep alone, BF16 and FP8); context rows
+(R = 17 .. 4096 rows through the input stage at once); the FP8 quantiser (once per weight load);
+an end-to-end figure through the host-buffer C entry point (host->device inputs and the draft
+back each step); SM clocks sampled during the timed loops; and the CPU oracle on bounded samples
+(BF16 and FP8 heads). The compact summaries come last on the line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --profile-case [--H 6144] [--V 32768] [--B 1] [--R 0] [--reps 3]   (for profilers)
 """
 from __future__ import annotations
 
@@ -55,19 +58,19 @@ SWEEP_SOURCES = [os.path.join(ROOT, "mtp_speculative_draft_head_gb300", "csrc", 
 
 
 # ------------------------------------------------------------------ algorithmic bytes
-def sweep_bytes(w_bytes: int, b: int = B, logits: bool = False) -> int:
+def sweep_bytes(w_bytes: int, b: int = B, logits: bool = False, h: int = H, v: int = V) -> int:
     """lm_head (+ FP8 row scales) read once, x and final_norm_w read, draft (+ logits) written."""
-    n = V * H * w_bytes + (V * 4 if w_bytes == 1 else 0) + b * H * 2 + H * 2 + b * 4
-    return n + (b * V * 4 if logits else 0)
+    n = v * h * w_bytes + (v * 4 if w_bytes == 1 else 0) + b * h * 2 + h * 2 + b * 4
+    return n + (b * v * 4 if logits else 0)
 
 
-def input_bytes(b: int = B) -> int:
+def input_bytes(b: int = B, h: int = H) -> int:
     """eh_proj read once, the embedding rows, target_hidden, two norm weights, x written, tokens."""
-    return H * 2 * H * 2 + b * H * 2 + b * H * 2 + 2 * H * 2 + b * H * 2 + b * 4
+    return h * 2 * h * 2 + b * h * 2 + b * h * 2 + 2 * h * 2 + b * h * 2 + b * 4
 
 
-def step_bytes(w_bytes: int) -> int:
-    return input_bytes() + sweep_bytes(w_bytes)
+def step_bytes(w_bytes: int, h: int = H, v: int = V) -> int:
+    return input_bytes(h=h) + sweep_bytes(w_bytes, h=h, v=v)
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -218,6 +221,64 @@ def capture(fn):
     return m.MtpDraftHead.capture(fn)
 
 
+# ------------------------------------------------------------------ the adversarial workload
+ADV_H, ADV_V, ADV_SEED = 4096, 131072, 7
+
+
+def adversarial_setup(m, dev, K, W, stream, status):
+    """Ties and outliers at H=4096, V=131072 (seed 7): lm_head ~ N(0, 0.02) with 1 % of its
+    elements scaled x50, then 64 rows set equal to 0.05 sign(x) so they tie for the maximum
+    (x = this workload's input-stage output; final_norm_w > 0 gives xhat the signs of x), and
+    target_hidden with 5 channels at +-100. Returns the CUDA graphs of K sweeps (BF16, FP8) and
+    of a K-step chain (BF16, FP8), the buffers they use, and the smallest planted row."""
+    w = synth.make_weights(ADV_H, ADV_V, ADV_SEED, dev)
+    w.lm_head = synth.add_outliers(w.lm_head, 0.01, 50.0, ADV_SEED)
+    tokens, hidden = synth.make_step_inputs(ADV_H, ADV_V, 1, ADV_SEED, dev)
+    hidden = synth.hidden_with_outlier_channels(hidden, 5, 100.0, ADV_SEED)
+    x = torch.empty((1, ADV_H), dtype=torch.bfloat16, device=dev)
+    m.mtp_head_input_batched(w.embed, w.enorm_w, w.hnorm_w, w.eh_proj, tokens, hidden, x, status, EPS)
+    rows = synth.pick_rows(ADV_V, 64, ADV_SEED, dev)
+    w.lm_head = synth.plant_rows(w.lm_head, rows, x[0])
+    head = m.MtpDraftHead(w.embed, w.lm_head, w.eh_proj, w.enorm_w, w.hnorm_w, w.final_norm_w, eps=EPS,
+                          max_batch=1)
+    if head.quantize_fp8() != 0:
+        raise RuntimeError("FP8 quantisation of the adversarial head failed")
+    tok = torch.empty((max(K, W) + 1, 1), dtype=torch.int32, device=dev)
+    tok[0].copy_(tokens)
+    d = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def sweep(n, fp8):
+        Wt, sc, wt = head._head(fp8)
+
+        def fn(st):
+            for _ in range(n):
+                m.mtp_head_logits_argmax_batched(x, head.final_norm_w, Wt, sc, wt, None, d, head.ws, status,
+                                                 EPS, st)
+        return fn
+
+    def chain(n, fp8):
+        Wt, sc, wt = head._head(fp8)
+
+        def fn(st):
+            for i in range(n):
+                m.mtp_head_forward_batched(head.embed, head.enorm_w, head.hnorm_w, head.eh_proj,
+                                           head.final_norm_w, Wt, sc, wt, tok[i], hidden, x, None, tok[i + 1],
+                                           head.ws, status, EPS, st)
+        return fn
+
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for fp8 in (False, True):
+            sweep(W, fp8)(stream)
+            chain(W, fp8)(stream)
+    torch.cuda.synchronize()
+    graphs = {}
+    for fp8 in (False, True):
+        graphs[("adv_sweep", fp8)] = capture(sweep(K, fp8))
+        graphs[("adv_chain", fp8)] = capture(chain(K, fp8))
+    return graphs, [head, w, tokens, hidden, x, tok, d], int(rows[0].item()), tok
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, world, rank, local):
     import mtp_speculative_draft_head_gb300 as m
@@ -259,6 +320,17 @@ def run_ours(args, world, rank, local):
                                                  EPS, st)
         return fn
 
+    lg1 = torch.empty((1, V), dtype=torch.float32, device=dev)
+
+    def sweep_logits_fn(n, fp8):
+        Wt, s, wt = head._head(fp8)
+
+        def fn(st):
+            for _ in range(n):
+                m.mtp_head_logits_argmax_batched(x, head.final_norm_w, Wt, s, wt, lg1, d, head.ws, status,
+                                                 EPS, st)
+        return fn
+
     def input_fn(n):
         def fn(st):
             for i in range(n):
@@ -274,10 +346,13 @@ def run_ours(args, world, rank, local):
         for fp8 in (False, True):
             chain_fn(W, fp8)(stream)
             sweep_fn(W, fp8)(stream)
+            sweep_logits_fn(W, fp8)(stream)
         input_fn(W)(stream)
     torch.cuda.synchronize()
     graphs = {("chain", False): capture(chain_fn(K, False)), ("chain", True): capture(chain_fn(K, True)),
               ("sweep", False): capture(sweep_fn(K, False)), ("sweep", True): capture(sweep_fn(K, True)),
+              ("sweep_logits", False): capture(sweep_logits_fn(K, False)),
+              ("sweep_logits", True): capture(sweep_logits_fn(K, True)),
               ("input", None): capture(input_fn(K))}
     torch.cuda.synchronize()
     for g in graphs.values():  # one untimed replay each
@@ -296,7 +371,8 @@ def run_ours(args, world, rank, local):
         tokb[0].copy_(tokens_b)
         xb = torch.empty((b, H), dtype=torch.bfloat16, device=dev)
         db = torch.empty(b, dtype=torch.int32, device=dev)
-        graph_buffers += [tokens_b, hidden_b, tokb, xb, db]
+        lgb = torch.empty((b, V), dtype=torch.float32, device=dev)
+        graph_buffers += [tokens_b, hidden_b, tokb, xb, db, lgb]
 
         def chain_b(n, fp8, tokb=tokb, hidden_b=hidden_b, xb=xb):
             Wt, s, wt = head._head(fp8)
@@ -308,13 +384,25 @@ def run_ours(args, world, rank, local):
                                                tokb[i + 1], head.ws, status, EPS, st)
             return fn
 
-        def sweep_b(n, fp8, xb=xb, db=db):
+        def sweep_b(n, fp8, xb=xb, db=db, lgb=lgb):  # logits stored, as the scope's sweep bytes count them
             Wt, s, wt = head._head(fp8)
 
             def fn(st):
                 for _ in range(n):
-                    m.mtp_head_logits_argmax_batched(xb, head.final_norm_w, Wt, s, wt, None, db, head.ws, status,
+                    m.mtp_head_logits_argmax_batched(xb, head.final_norm_w, Wt, s, wt, lgb, db, head.ws, status,
                                                      EPS, st)
+            return fn
+
+        cwsb = m.context_workspace(b, H, dev)
+        graph_buffers.append(cwsb)
+
+        # the input stage alone as the chain runs it: with room for a prebuilt concat (built once by
+        # the row-parallel kernel for B >= 6), which the context-row entry point gives it at R <= 16
+        def input_b(n, tokb=tokb, hidden_b=hidden_b, xb=xb, cwsb=cwsb):
+            def fn(st):
+                for i in range(n):
+                    m.mtp_head_context_rows(head.embed, head.enorm_w, head.hnorm_w, head.eh_proj, tokb[i % 2],
+                                            hidden_b, xb, cwsb, status, EPS, st)
             return fn
 
         stream.wait_stream(torch.cuda.current_stream())  # inputs were drawn on the current stream
@@ -322,10 +410,12 @@ def run_ours(args, world, rank, local):
             for fp8 in (False, True):
                 chain_b(max(W, 3), fp8)(stream)
                 sweep_b(max(W, 3), fp8)(stream)
+            input_b(max(W, 3))(stream)
         torch.cuda.synchronize()
         for fp8 in (False, True):
             bgraphs[(b, "chain", fp8)] = capture(chain_b(Kb, fp8))
             bgraphs[(b, "sweep", fp8)] = capture(sweep_b(Kb, fp8))
+        bgraphs[(b, "input", None)] = capture(input_b(Kb))
     # context rows (prefill / catch-up): R rows through the input stage at once, concat kernel +
     # tcgen05 GEMM, Kb calls per graph
     cgraphs = {}
@@ -365,13 +455,48 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     qgraph = capture(quant_fn(Kq))
     torch.cuda.synchronize()
-    for g in list(bgraphs.values()) + list(cgraphs.values()) + [qgraph]:
+    agraphs, adv_keep, adv_first_planted, adv_tok = adversarial_setup(m, dev, K, W, stream, status)
+    graph_buffers += adv_keep
+    # the vocabulary split in two (the source's sharded head on two ranks, here both halves on
+    # this GPU): each half's sweep alone -- what one rank runs -- and the pick from the two keys
+    shard_keys = torch.empty((2, 1), dtype=torch.int64, device=dev)
+    shard_draft = torch.empty(1, dtype=torch.int32, device=dev)
+    shards = [m.VocabShard(w.lm_head, w.final_norm_w, r, 2, eps=EPS, max_batch=1) for r in range(2)]
+    for vs in shards:
+        vs.lm_head_fp8 = head.lm_head_fp8[vs.v0:vs.v0 + vs.n]  # the rows of the full FP8 copy are the shard's copy
+        vs.row_scale = head.row_scale[vs.v0:vs.v0 + vs.n]
+    graph_buffers += [shard_keys, shard_draft, shards]
+
+    def half_sweep(n, fp8, r):
+        def fn(st):
+            for _ in range(n):
+                shards[r].picks(x, fp8=fp8, pick=shard_keys[r], status=status, stream=st)
+        return fn
+
+    def pick_fn(n):
+        def fn(st):
+            for _ in range(n):
+                m.mtp_head_pick_combine(shard_keys, shard_draft, stream=st)
+        return fn
+
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for fp8 in (False, True):
+            for r in range(2):
+                half_sweep(W, fp8, r)(stream)
+        pick_fn(W)(stream)
+    torch.cuda.synchronize()
+    sgraphs = {("half", fp8): capture(half_sweep(K, fp8, 1)) for fp8 in (False, True)}
+    sgraphs[("pick", None)] = capture(pick_fn(K))
+    for g in list(bgraphs.values()) + list(cgraphs.values()) + [qgraph] + list(agraphs.values()) + \
+            list(sgraphs.values()):
         g.replay()
     torch.cuda.synchronize()
 
     launches_all = 0
     with ClockSampler(local) as clocks:
-        for key in (("chain", False), ("chain", True), ("sweep", False), ("sweep", True), ("input", None)):
+        for key in (("chain", False), ("chain", True), ("sweep", False), ("sweep", True), ("sweep_logits", False),
+                    ("sweep_logits", True), ("input", None)):
             barrier(world)
             ms = timed_graph(graphs[key], torch.cuda.current_stream())
             barrier(world)
@@ -381,7 +506,7 @@ def run_ours(args, world, rank, local):
             barrier(world)
             results[key] = timed_graph(g, torch.cuda.current_stream())
             barrier(world)
-            launches_all += 2 * Kb if key[1] == "chain" else Kb
+            launches_all += 2 * Kb if key[1] == "chain" else Kb  # (B >= 6 input stages: 2 kernels, not counted)
         for r, g in cgraphs.items():
             barrier(world)
             results[("context", r)] = timed_graph(g, torch.cuda.current_stream())
@@ -391,6 +516,16 @@ def run_ours(args, world, rank, local):
         results["quantize"] = timed_graph(qgraph, torch.cuda.current_stream())
         barrier(world)
         launches_all += Kq
+        for key, g in agraphs.items():
+            barrier(world)
+            results[key] = timed_graph(g, torch.cuda.current_stream())
+            barrier(world)
+            launches_all += 2 * K if key[0] == "adv_chain" else K
+        for key, g in sgraphs.items():
+            barrier(world)
+            results[key] = timed_graph(g, torch.cuda.current_stream())
+            barrier(world)
+            launches_all += K
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}: {m.strerror(int(status.item()))}")
     drafts = tok[1:K + 1].view(-1)
@@ -399,8 +534,6 @@ def run_ours(args, world, rank, local):
 
     bf = aggregate(results[("chain", False)], step_bytes(2), K, world)
     f8 = aggregate(results[("chain", True)], step_bytes(1), K, world)
-    sw_bf = aggregate(results[("sweep", False)], sweep_bytes(2), K, world)
-    sw_f8 = aggregate(results[("sweep", True)], sweep_bytes(1), K, world)
     inp = aggregate(results[("input", None)], input_bytes(), K, world)
 
     # end to end through the host-buffer entry point: inputs copied in and the draft copied out
@@ -435,22 +568,24 @@ def run_ours(args, world, rank, local):
         e = {}
         for fp8, tag, wb in ((False, "bf16", 2), (True, "fp8", 1)):
             ch = aggregate(results[(b, "chain", fp8)], input_bytes(b) + sweep_bytes(wb, b), Kb, world)
-            sw = aggregate(results[(b, "sweep", fp8)], sweep_bytes(wb, b), Kb, world)
+            sw = aggregate(results[(b, "sweep", fp8)], sweep_bytes(wb, b, logits=True), Kb, world)
             e[f"head_{tag}_us"] = round(ch["ms_per_step"] * 1e3, 2)
             e[f"tokens_per_s_{tag}"] = round(b * world / (ch["ms_per_step"] * 1e-3), 1)
             e[f"sweep_{tag}_us"] = round(sw["ms_per_step"] * 1e3, 2)
             e[f"sweep_{tag}_gbs"] = round(sw["gbs"], 1)
             e[f"sweep_{tag}_frac"] = round(sw["gbs"] / world / peak, 4)
-        e["input_us_approx"] = round(e["head_bf16_us"] - e["sweep_bf16_us"], 2)
+        ti = aggregate(results[(b, "input", None)], input_bytes(b), Kb, world)
+        e["input_us"] = round(ti["ms_per_step"] * 1e3, 2)
+        e["input_frac"] = round(ti["gbs"] / world / peak, 4)
         batched[f"B={b}"] = e
     tc_peak, tc_src = peak_bf16()
     context = {}
     for r in CONTEXT_ROWS:
-        us = max_over_ranks(results[("context", r)] / Kb, world) * 1e3
+        t_us = max_over_ranks(results[("context", r)] / Kb, world) * 1e3
         flops = 2.0 * r * H * 2 * H
-        context[f"R={r}"] = {"us": round(us, 2), "rows_per_s": round(r * world / (us * 1e-6), 1),
-                             "tflops": round(flops / (us * 1e-6) / 1e12, 1),
-                             "frac": round(flops / (us * 1e-6) / 1e12 / tc_peak, 4)}
+        context[f"R={r}"] = {"us": round(t_us, 2), "rows_per_s": round(r * world / (t_us * 1e-6), 1),
+                             "tflops": round(flops / (t_us * 1e-6) / 1e12, 1),
+                             "frac": round(flops / (t_us * 1e-6) / 1e12 / tc_peak, 4)}
     q_us = max_over_ranks(results["quantize"] / Kq, world) * 1e3
     q_bytes = V * H * 2 + V * H + V * 4  # read the BF16 head, write codes and scales
     quantize = {"us": round(q_us, 1), "gbs": round(q_bytes / (q_us * 1e-6) / 1e9, 1),
@@ -458,8 +593,30 @@ def run_ours(args, world, rank, local):
                 "timing": "Kq calls in one CUDA graph (each reads the 1.9 GB head, above L2); frac of the "
                           "measured copy peak",
                 "kernel": "quantize_vec_kernel (offline: once per weight load)"}
+
+    def us(key, n=K):
+        return max_over_ranks(results[key] / n, world) * 1e3
+
+    def frac(nbytes, t_us):
+        return round(nbytes / (t_us * 1e-6) / 1e9 / peak, 4)
+
+    # the sweep's roofline is taken on the launch that stores the logits: the scope's algorithmic
+    # bytes of a sweep include B * V * 4 of FP32 logits (the draft-only launch is reported beside it)
     kname = "sweep_regx_kernel<BF16,H=6144,B=1>"
-    achieved = sweep_bytes(2) / (results[("sweep", False)] / K * 1e-3) / 1e9
+    kname8 = "sweep_regx_kernel<FP8,H=6144,B=1>"
+    bf_lg_us, f8_lg_us = us(("sweep_logits", False)), us(("sweep_logits", True))
+    bf_us, f8_us = us(("sweep", False)), us(("sweep", True))
+    achieved = sweep_bytes(2, logits=True) / (bf_lg_us * 1e-6) / 1e9
+    achieved8 = sweep_bytes(1, logits=True) / (f8_lg_us * 1e-6) / 1e9
+    adv_first_ok = bool((adv_tok[1:K + 1].view(-1) == adv_first_planted).all())
+    adv = {"H": ADV_H, "V": ADV_V}
+    for fp8, tag, wb in ((False, "bf16", 2), (True, "fp8", 1)):
+        t = us(("adv_sweep", fp8))
+        adv[f"sweep_{tag}_us"] = round(t, 2)
+        adv[f"sweep_{tag}_frac"] = frac(sweep_bytes(wb, h=ADV_H, v=ADV_V), t)
+        adv[f"head_{tag}_us"] = round(us(("adv_chain", fp8)), 2)
+    adv["drafts_smallest_planted_row"] = adv_first_ok
+    b16 = batched["B=16"]
     line = {
         "metric": METRIC,
         "value": round(bf["gbs"], 1),
@@ -480,19 +637,17 @@ def run_ours(args, world, rank, local):
                    "H": H, "V": V, "B": B, "eps": EPS, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (2.06 GB of weights streamed per step, L2 129 MB)",
                    "bytes_per_step": step_bytes(2)},
-        "stages": {"input_us": round(inp["ms_per_step"] * 1e3, 2), "input_gbs": round(inp["gbs"], 1),
-                   "sweep_bf16_us": round(sw_bf["ms_per_step"] * 1e3, 2), "sweep_bf16_gbs": round(sw_bf["gbs"], 1),
-                   "sweep_fp8_us": round(sw_f8["ms_per_step"] * 1e3, 2), "sweep_fp8_gbs": round(sw_f8["gbs"], 1)},
-        "fp8": {"us_per_step": round(f8["ms_per_step"] * 1e3, 2), "value": round(f8["gbs"], 1),
-                "unit": "GB/s", "bytes_per_step": step_bytes(1),
-                "sweep_roofline_frac": round(sweep_bytes(1) / (results[("sweep", True)] / K * 1e-3) / 1e9 / peak, 4)},
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kname),
-                     "bytes_per_launch": sweep_bytes(2), "peak_source": peak_src,
-                     "timing": "K back-to-back launches in one CUDA graph, CUDA events on the launching stream"},
+                     "bytes_per_launch": sweep_bytes(2, logits=True), "peak_source": peak_src,
+                     "timing": "K back-to-back launches (logits stored) in one CUDA graph, CUDA events on the "
+                               "launching stream"},
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "us_per_step": round(e2e_ms / ke * 1e3, 2),
                 "h2d_bytes_per_step": 4 + H * 2, "d2h_bytes_per_step": 4, "steps": ke,
                 "api": "mtp_head_forward_host through HostStep (pinned host buffers, synchronous per step)"},
+        "gpu_launches": 2 * K,  # the BF16 chain region `value` is timed on: 2 kernels per step
+        "gpu_launches_all_timed_regions": launches_all,
+        "clocks": clocks.summary(),
         "batched": dict(batched, steps=Kb, kernels="tensor-core input stage and sweep (mma.sync)",
                         timing="Kb-step chains / sweep loops in one CUDA graph each; frac of the measured peak"),
         "context": dict(context, steps=Kb, peak_tflops=tc_peak, peak_source=tc_src,
@@ -500,14 +655,34 @@ def run_ours(args, world, rank, local):
                         timing="Kb calls in one CUDA graph; TFLOP/s of the GEMM (2 R H 2H) over the time of both "
                                "kernels; frac of the measured bf16 burst peak"),
         "quantize_fp8": quantize,
-        "gpu_launches": 2 * K,  # the BF16 chain region `value` is timed on: 2 kernels per step
-        "gpu_launches_all_timed_regions": launches_all,
-        "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, hiddens, first, seconds=args.cpu_seconds)
         line["cpu_baseline_all_cores"] = cpu_baseline(w, hiddens, first, seconds=args.cpu_seconds / 2,
                                                       threads=os.cpu_count() or 1)
+        line["cpu_baseline_fp8"] = cpu_baseline(w, hiddens, first, seconds=args.cpu_seconds / 2,
+                                                fp8=(head.lm_head_fp8, head.row_scale))
+    # compact summaries last, so that a reader keeping only the end of the line still has them
+    line["stages"] = {"input_us": round(inp["ms_per_step"] * 1e3, 2),
+                      "input_frac": frac(input_bytes(), inp["ms_per_step"] * 1e3),
+                      "sweep_bf16_us": round(bf_us, 2), "sweep_bf16_frac": frac(sweep_bytes(2), bf_us),
+                      "sweep_bf16_logits_us": round(bf_lg_us, 2),
+                      "sweep_fp8_us": round(f8_us, 2), "sweep_fp8_frac": frac(sweep_bytes(1), f8_us),
+                      "sweep_fp8_logits_us": round(f8_lg_us, 2),
+                      "head_bf16_us": round(bf["ms_per_step"] * 1e3, 2), "head_fp8_us": round(f8["ms_per_step"] * 1e3, 2)}
+    line["fp8_b1"] = {"kernel": kname8, "us": round(f8_lg_us, 2), "achieved": round(achieved8, 1), "peak": peak,
+                      "frac": round(achieved8 / peak, 4), "bytes_per_launch": sweep_bytes(1, logits=True),
+                      "traffic": recorded_traffic(kname8), "logits": "stored"}
+    line["adversarial"] = adv
+    line["b16"] = {k: b16[k] for k in ("sweep_bf16_us", "sweep_bf16_frac", "sweep_fp8_us", "sweep_fp8_frac",
+                                       "input_us", "input_frac")}
+    half_v = shards[1].n
+    line["shard2"] = {"rows": half_v}
+    for fp8, tag, wb in ((False, "bf16", 2), (True, "fp8", 1)):
+        t = us(("half", fp8))
+        line["shard2"][f"half_sweep_{tag}_us"] = round(t, 2)
+        line["shard2"][f"half_sweep_{tag}_frac"] = frac(sweep_bytes(wb, v=half_v), t)
+    line["shard2"]["pick_us"] = round(us(("pick", None)), 2)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -516,8 +691,9 @@ def run_ours(args, world, rank, local):
 SAMPLE_DIV = 64  # one sample = 1/64 of a draft step's rows (both GEMVs), norms in full
 
 
-def _oracle_sample_setup(w, hiddens, first, n_slices: int):
-    """Host copies of what the samples touch: eh_proj, the needed lm_head slices, norms."""
+def _oracle_sample_setup(w, hiddens, first, n_slices: int, fp8=None):
+    """Host copies of what the samples touch: eh_proj, the needed lm_head slices (of the FP8
+    copy and its row scales when fp8 = (codes, scales) is given), norms."""
     wb = {k: synth.bits(getattr(w, k)) for k in ("enorm_w", "hnorm_w", "final_norm_w", "eh_proj")}
     tok = int(first.item())
     wb["embed_row"] = synth.bits(w.embed[tok])
@@ -525,14 +701,18 @@ def _oracle_sample_setup(w, hiddens, first, n_slices: int):
     slices = []
     for j in range(n_slices):
         v0 = (j * 7919 % SAMPLE_DIV) * rows
-        slices.append((v0, synth.bits(w.lm_head[v0:v0 + rows])))
+        if fp8 is None:
+            slices.append((v0, synth.bits(w.lm_head[v0:v0 + rows]), None))
+        else:
+            slices.append((v0, synth.bits(fp8[0][v0:v0 + rows]), fp8[1][v0:v0 + rows].cpu().numpy()))
     return wb, slices, [synth.bits(hiddens[i % hiddens.shape[0]]) for i in range(n_slices)]
 
 
-def oracle_sample_step(wb, lm_slice, hidden_bits, j, threads: int = 1):
+def oracle_sample_step(wb, lm_slice, hidden_bits, j, threads: int = 1, scale_slice=None):
     """1/64 of one draft step on the oracle: enorm, hnorm and the final norm in full, 1/64 of the
-    eh_proj rows and 1/64 of the vocabulary (row ranges split over `threads` host threads);
-    returns the algorithmic bytes it covered."""
+    eh_proj rows and 1/64 of the vocabulary (row ranges split over `threads` host threads; the
+    FP8 head's codes and scales when scale_slice is given); returns the algorithmic bytes it
+    covered."""
     import oracle
     c = np.concatenate([oracle.rms_norm(wb["embed_row"], wb["enorm_w"], EPS),
                         oracle.rms_norm(hidden_bits.reshape(-1), wb["hnorm_w"], EPS)])
@@ -542,30 +722,34 @@ def oracle_sample_step(wb, lm_slice, hidden_bits, j, threads: int = 1):
     x = np.zeros(H, np.uint16)
     x[n0:n0 + r] = xs
     xhat = oracle.final_norm(x, wb["final_norm_w"], EPS)
-    lg = oracle.logits(0, lm_slice, None, xhat, threads=threads)
+    if scale_slice is None:
+        lg = oracle.logits(0, lm_slice, None, xhat, threads=threads)
+    else:
+        lg = oracle.logits(1, lm_slice, scale_slice, xhat, threads=threads)
     oracle.argmax(lg)
-    return step_bytes(2) / SAMPLE_DIV
+    return step_bytes(2 if scale_slice is None else 1) / SAMPLE_DIV
 
 
-def cpu_baseline(w, hiddens, first, seconds: float = 12.0, threads: int = 1) -> dict:
+def cpu_baseline(w, hiddens, first, seconds: float = 12.0, threads: int = 1, fp8=None) -> dict:
     import oracle
     oracle.build()
     n_slices = 8
-    wb, slices, hb = _oracle_sample_setup(w, hiddens, first, n_slices)
+    wb, slices, hb = _oracle_sample_setup(w, hiddens, first, n_slices, fp8)
     t0 = time.perf_counter()
     done, nbytes, j = 0, 0.0, 0
     while True:
-        v0, sl = slices[j % n_slices]
-        nbytes += oracle_sample_step(wb, sl, hb[j % n_slices], j, threads)
+        v0, sl, sc = slices[j % n_slices]
+        nbytes += oracle_sample_step(wb, sl, hb[j % n_slices], j, threads, sc)
         done += 1
         j += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
     who = "one thread" if threads == 1 else f"{threads} threads (row ranges split, the oracle's own option)"
+    head = "BF16 head" if fp8 is None else "FP8 head (codes and row scales)"
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{done} samples of 1/{SAMPLE_DIV} of a draft step each (eh_proj and lm_head row "
-                      f"slices, norms in full), fp64 C oracle, {who}, {dt:.1f} s",
+            "sample": f"{done} samples of 1/{SAMPLE_DIV} of a draft step each ({head}; eh_proj and lm_head row "
+                      f"slices, norms in full), fp64 scalar C oracle built -O2 (not tuned), {who}, {dt:.1f} s",
             "us_per_step_equiv": round(dt / done * SAMPLE_DIV * 1e6, 1)}
 
 
@@ -591,7 +775,8 @@ def run_reference(args, world, rank):
     dt = time.perf_counter() - t0
     gbs = nbytes / dt / 1e9
     sample = (f"each step = 1/{SAMPLE_DIV} of a draft step (eh_proj and lm_head row slices, norms in full), "
-              f"fp64 C oracle, {threads} threads (row ranges split, the oracle's own option)")
+              f"fp64 scalar C oracle built -O2 (not tuned), {threads} threads (row ranges split, the oracle's "
+              f"own option)")
     line = {"metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
@@ -604,6 +789,39 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ profiler case
+def profile_case(args):
+    """A small, self-contained run for profilers (ncu) and quick timing, not a bench line:
+    seeded synthetic weights of hidden size --H and vocabulary --V on the GPU, the FP8 copy, then
+    --reps draft steps of --B sequences with the BF16 head and --reps with the FP8 head (input
+    stage + output stage each); with --R, --reps context-row input stages over R rows instead.
+    The default V (32768) keeps the BF16 lm_head (403 MB) above the L2 size while the run holds
+    about 1.3 GB on the device, so a multi-pass capture of one launch ends in seconds."""
+    import mtp_speculative_draft_head_gb300 as m
+    dev = torch.device("cuda:0")
+    w = synth.make_weights(args.H, args.V, 0, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if args.R:
+        tokens, hidden = synth.make_step_inputs(args.H, args.V, args.R, 2, dev, distinct=False)
+        x = torch.empty((args.R, args.H), dtype=torch.bfloat16, device=dev)
+        ws = m.context_workspace(args.R, args.H, dev)
+        for _ in range(args.reps):
+            m.mtp_head_context_rows(w.embed, w.enorm_w, w.hnorm_w, w.eh_proj, tokens, hidden, x, ws, status)
+    else:
+        head = m.MtpDraftHead(w.embed, w.lm_head, w.eh_proj, w.enorm_w, w.hnorm_w, w.final_norm_w,
+                              max_batch=args.B)
+        if head.quantize_fp8() != 0:
+            raise RuntimeError("FP8 quantisation failed")
+        tokens, hidden = synth.make_step_inputs(args.H, args.V, args.B, 1, dev)
+        for _ in range(args.reps):
+            for fp8 in (False, True):
+                head.forward(tokens, hidden, fp8=fp8, status=status)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    print("ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -612,7 +830,16 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile-case", action="store_true", help="a small run for profilers (no bench line)")
+    ap.add_argument("--H", type=int, default=6144, help="--profile-case: hidden size")
+    ap.add_argument("--V", type=int, default=32768, help="--profile-case: vocabulary size")
+    ap.add_argument("--B", type=int, default=1, help="--profile-case: sequences per step")
+    ap.add_argument("--R", type=int, default=0, help="--profile-case: context rows instead of draft steps")
+    ap.add_argument("--reps", type=int, default=3, help="--profile-case: repetitions")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world, rank, local = dist_setup()
