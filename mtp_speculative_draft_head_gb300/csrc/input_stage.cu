@@ -8,13 +8,15 @@
 // builds the normalised concat of its B sequences in shared memory (one pass, one block
 // reduction for all 2B norms) while its first weight stages are already in flight.
 //
-// Accuracy: x is rounded to BF16 right after this sum, so the sum is error-free up to the final
-// rounding: every product of two BF16 values is exact in fp32, and each one is added to a
-// double-float (hi, lo) with TwoSum -- four packed f32x2 double-floats per lane and sequence,
-// element pair (2u, 2u+1) of a 16-byte vector going to pair u; the eight double-floats and
-// then the lanes are combined the same way and the value is rounded once to BF16. x therefore
-// equals the BF16 rounding of the exact sum unless that lies within ~2^-40 (relative) of a
-// rounding midpoint.
+// Accuracy: the source's eh_proj gemv accumulates in FP32, and so does this kernel. Every
+// product of two BF16 values is exact in fp32 (mixed-precision FMA); each lane keeps eight FP32
+// accumulators per sequence (element e of a 16-byte vector goes to accumulator e), so an
+// accumulator sums n = ceil(H / 128) exact products one FP32 rounding at a time. The 8 x 32
+// accumulator values of a row are then added error-free (double-float TwoSum) and rounded once
+// to BF16. x is therefore the BF16 rounding of a value within (n - 1) * 2^-24 * sum_k |w_k c_k|
+// (first order) of the exact sum: at H = 6144, n = 48 and the band is below 2^-18.4 of the sum
+// of |products|. An error-free sum of every product (TwoSum per product) had cost 5 us of a 30 us
+// launch at the GLM size: the kernel is issue-bound there, not HBM-bound.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -64,25 +66,24 @@ __device__ void build_concat(const InputArgs& a, int b0, int nb, uint16_t* vec, 
   __syncthreads();
 }
 
-// Exact products of one 16-byte weight vector (4 BF16 pairs) with the concat, added to the
-// four packed double-floats of one sequence (independent chains).
-__device__ __forceinline__ void dot8_exact(const uint4& w, const uint4& c, DF2 (&acc)[4]) {
+// One 16-byte weight vector (4 BF16 pairs) times the matching concat vector: element 2u goes to
+// acc[2u], element 2u + 1 to acc[2u + 1], each an FMA with the exact product and one fp32
+// rounding (mixed BF16 x BF16 -> FP32), eight independent chains.
+__device__ __forceinline__ void dot8_fp32(const uint4& w, const uint4& c, float (&acc)[8]) {
   const uint32_t wu[4] = {w.x, w.y, w.z, w.w};
   const uint32_t cu[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
 #if MTP_MIXED_FMA
-    float p0, p1;
-    asm("{\n\t.reg .b16 wl, wh, cl, ch;\n\t.reg .f32 z;\n\t"
-        "mov.b32 {wl, wh}, %2;\n\tmov.b32 {cl, ch}, %3;\n\tmov.f32 z, 0f00000000;\n\t"
-        "fma.rn.f32.bf16 %0, wl, cl, z;\n\tfma.rn.f32.bf16 %1, wh, ch, z;\n\t}"
-        : "=f"(p0), "=f"(p1)
+    asm("{\n\t.reg .b16 wl, wh, cl, ch;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\tmov.b32 {cl, ch}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, wl, cl, %0;\n\tfma.rn.f32.bf16 %1, wh, ch, %1;\n\t}"
+        : "+f"(acc[2 * u]), "+f"(acc[2 * u + 1])
         : "r"(wu[u]), "r"(cu[u]));
-    const uint64_t p = f2_pack(p0, p1);
 #else
-    const uint64_t p = f2_mul(bf16x2_to_f2(wu[u]), bf16x2_to_f2(cu[u]));  // exact products
+    acc[2 * u] = __fmaf_rn(bf16_lo(wu[u]), bf16_lo(cu[u]), acc[2 * u]);
+    acc[2 * u + 1] = __fmaf_rn(bf16_hi(wu[u]), bf16_hi(cu[u]), acc[2 * u + 1]);
 #endif
-    df2_add(acc[u], p);
   }
 }
 
@@ -164,21 +165,21 @@ __global__ void __launch_bounds__(NWI * 32, 1) input_tma_kernel(const InputArgs 
 
   // partial sums of rows split between two warps: [warp][first | last][sequence]
   DF* part = reinterpret_cast<DF*>(red);
-  const uint64_t zero2 = f2_pack(0.0f, 0.0f);
-  DF2 acc[NB][4];
+  float acc[NB][8];
 #pragma unroll
   for (int b = 0; b < NB; ++b)
 #pragma unroll
-    for (int u = 0; u < 4; ++u) acc[b][u] = DF2{zero2, zero2};
+    for (int e = 0; e < 8; ++e) acc[b][e] = 0.0f;
   int cs = 0, t_fail = -1;
   uint32_t parity = 0;
+  // the row's 8 x 32 accumulator values, added as double-floats (relative error ~2^-44)
   auto row_total = [&](int b) {
-    DF v = df_add(df_add(df_add(df2_x(acc[b][0]), df2_y(acc[b][0])), df_add(df2_x(acc[b][1]), df2_y(acc[b][1]))),
-                  df_add(df_add(df2_x(acc[b][2]), df2_y(acc[b][2])), df_add(df2_x(acc[b][3]), df2_y(acc[b][3]))));
+    DF v = df_add(df_add(df_add(DF{acc[b][0], 0.0f}, DF{acc[b][1], 0.0f}), df_add(DF{acc[b][2], 0.0f}, DF{acc[b][3], 0.0f})),
+                  df_add(df_add(DF{acc[b][4], 0.0f}, DF{acc[b][5], 0.0f}), df_add(DF{acc[b][6], 0.0f}, DF{acc[b][7], 0.0f})));
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) v = df_add(v, shfl_xor_df(v, m));
 #pragma unroll
-    for (int u = 0; u < 4; ++u) acc[b][u] = DF2{zero2, zero2};
+    for (int e = 0; e < 8; ++e) acc[b][e] = 0.0f;
     return v;
   };
   for (int t = 0; t < nitems; ++t) {
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(NWI * 32, 1) input_tma_kernel(const InputArgs 
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         const uint4 cq = reinterpret_cast<const uint4*>(vec + static_cast<size_t>(b) * vec_elems)[J0 + j];
-        dot8_exact(q, cq, acc[b]);
+        dot8_fp32(q, cq, acc[b]);
       }
     }
     __syncwarp();

@@ -11,7 +11,7 @@ import torch
 import mtp_speculative_draft_head_gb300 as m
 import oracle
 import synth
-from gpu_helpers import TOL_BF16, TOL_FP8, abs_product_sums, check_draft, check_logits_and_draft, check_x
+from gpu_helpers import TOL_BF16, TOL_FP8, abs_product_sums, check_draft, check_logits_and_draft, check_x, x_band
 
 pytestmark = pytest.mark.gpu
 
@@ -40,12 +40,11 @@ class Model:
         self.sb = self.head.row_scale.cpu().numpy()
 
     def oracle_x(self, tokens, hidden):
-        """(x, status, sums, band sums): the last is None for one sequence (error-free sum)."""
+        """(x, status, sums, sums of |products|) -- the last scales the accumulation band of x."""
         x, concat, st, sums = oracle.input_stage(self.wb["embed"], self.wb["enorm_w"], self.wb["hnorm_w"],
                                                  self.wb["eh_proj"], _bits(tokens).astype(np.int64), _bits(hidden),
                                                  EPS, return_concat=True, return_sums=True)
-        abs_sums = abs_product_sums(self.wb["eh_proj"], concat) if x.shape[0] >= 2 else None
-        return x, st, sums, abs_sums
+        return x, st, sums, abs_product_sums(self.wb["eh_proj"], concat)
 
     def oracle_logits(self, x_bits, fp8):
         xhat = oracle.final_norm(x_bits, self.wb["final_norm_w"], EPS)
@@ -83,7 +82,7 @@ def test_glm_head(glm, B, fp8):
     assert int(status.item()) == 0
     x_ref, st, sums, abs_sums = glm.oracle_x(tokens, hidden)
     assert np.all(st == 0)
-    n_diff = check_x(_bits(x), x_ref, sums, abs_sums)
+    n_diff = check_x(_bits(x), x_ref, sums, abs_sums, x_band(glm.H, B))
     # the band is a worst-case bound; the FP32 runs differ from the exact sum far more rarely
     assert n_diff <= max(1, x_ref.size // 100)
     ref = glm.oracle_logits(x_ref, fp8)
@@ -135,7 +134,7 @@ def test_adversarial_ties_and_outliers():
     md = Model(H, V, seed, outliers=True)
     tokens, hidden = synth.make_step_inputs(H, V, 1, seed, DEV)
     hidden = synth.hidden_with_outlier_channels(hidden, 5, 100.0, seed)
-    x_ref, _, sums, _ = md.oracle_x(tokens, hidden)
+    x_ref, _, sums, abs_sums = md.oracle_x(tokens, hidden)
     xhat = oracle.final_norm(x_ref, md.wb["final_norm_w"], EPS)[0]
     rows = synth.pick_rows(V, 64, seed, DEV)
     md.w.lm_head = synth.plant_rows(md.w.lm_head, rows, torch.from_numpy(oracle.bf16_to_f64(xhat)))
@@ -146,7 +145,8 @@ def test_adversarial_ties_and_outliers():
     for fp8 in (False, True):
         x, logits, draft = md.head.forward(tokens, hidden, fp8=fp8, logits=True)
         torch.cuda.synchronize()
-        check_x(_bits(x), x_ref, sums)
+        n_diff = check_x(_bits(x), x_ref, sums, abs_sums, x_band(H, 1))
+        assert n_diff <= max(1, x_ref.size // 100)
         lg = logits.cpu().view(-1)
         assert len(set(lg[planted].view(torch.int32).tolist())) == 1
         assert int(draft.item()) == planted[0]

@@ -12,7 +12,7 @@ import torch
 import mtp_speculative_draft_head_gb300 as m
 import oracle
 import synth
-from gpu_helpers import (TOL_BF16, TOL_FP8, abs_product_sums, check_draft, check_logits_and_draft, check_x,
+from gpu_helpers import (TOL_BF16, TOL_FP8, abs_product_sums, check_draft, check_logits_and_draft, check_x, x_band,
                          lowest_argmax)
 
 pytestmark = pytest.mark.gpu
@@ -69,8 +69,8 @@ class Case:
         return x, st, sums
 
     def abs_sums(self):
-        """Band of the batched input stage (None for one sequence: error-free sum)."""
-        return abs_product_sums(self.wb["eh_proj"], self.concat_ref) if self.B >= 2 else None
+        """sum_k |eh_proj[h, k] * concat[b, k]|: the scale of the accumulation band of x."""
+        return abs_product_sums(self.wb["eh_proj"], self.concat_ref)
 
     def oracle_logits(self, x_bits, wt, W_bits, scale):
         xhat = oracle.final_norm(x_bits, self.wb["final_norm_w"], EPS)
@@ -109,7 +109,7 @@ def test_head_matches_oracle(H, V, B, fp8):
     assert np.all(st_ref == 0)
     x_gpu, st = c.input_gpu()
     assert st == 0
-    check_x(_bits(x_gpu), x_ref, sums, c.abs_sums())
+    check_x(_bits(x_gpu), x_ref, sums, c.abs_sums(), x_band(H, B))
     if fp8:
         q, s, qst = c.quantize_gpu()
         assert qst == 0
