@@ -19,7 +19,7 @@ back each step); SM clocks sampled during the timed loops; and the CPU oracle on
 (BF16 and FP8 heads). The compact summaries come last on the line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --profile-case [--H 6144] [--V 32768] [--B 1] [--R 0] [--reps 3]   (for profilers)
+  python bench.py --profile-case [--H 6144] [--V 32768] [--B 1] [--R 0] [--reps 3] [--logits]   (for profilers)
 """
 from __future__ import annotations
 
@@ -360,7 +360,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     # batched drafting (B sequences per step, one pass over the weights): a shorter chain of
     # Kb steps per B, BF16 and FP8, plus the sweep alone
-    Kb = max(1, min(K, 20))
+    Kb = 50  # launches per graph of the batched and context-row sections (independent of K)
     bgraphs = {}
     # a captured graph holds raw device pointers, not the tensors: every buffer a graph uses stays
     # referenced here until the end of the run
@@ -794,7 +794,8 @@ def profile_case(args):
     """A small, self-contained run for profilers (ncu) and quick timing, not a bench line:
     seeded synthetic weights of hidden size --H and vocabulary --V on the GPU, the FP8 copy, then
     --reps draft steps of --B sequences with the BF16 head and --reps with the FP8 head (input
-    stage + output stage each); with --R, --reps context-row input stages over R rows instead.
+    stage + output stage each, logits stored with --logits); with --R, --reps context-row input
+    stages over R rows instead.
     The default V (32768) keeps the BF16 lm_head (403 MB) above the L2 size while the run holds
     about 1.3 GB on the device, so a multi-pass capture of one launch ends in seconds."""
     import mtp_speculative_draft_head_gb300 as m
@@ -815,7 +816,7 @@ def profile_case(args):
         tokens, hidden = synth.make_step_inputs(args.H, args.V, args.B, 1, dev)
         for _ in range(args.reps):
             for fp8 in (False, True):
-                head.forward(tokens, hidden, fp8=fp8, status=status)
+                head.forward(tokens, hidden, fp8=fp8, logits=args.logits, status=status)
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
@@ -836,6 +837,7 @@ def main():
     ap.add_argument("--B", type=int, default=1, help="--profile-case: sequences per step")
     ap.add_argument("--R", type=int, default=0, help="--profile-case: context rows instead of draft steps")
     ap.add_argument("--reps", type=int, default=3, help="--profile-case: repetitions")
+    ap.add_argument("--logits", action="store_true", help="--profile-case: store the logits")
     args = ap.parse_args()
     if args.profile_case:
         profile_case(args)

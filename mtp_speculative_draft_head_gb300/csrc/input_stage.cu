@@ -15,7 +15,7 @@
 // accumulator values of a row are then added error-free (double-float TwoSum) and rounded once
 // to BF16. x is therefore the BF16 rounding of a value within (n - 1) * 2^-24 * sum_k |w_k c_k|
 // (first order) of the exact sum: at H = 6144, n = 48 and the band is below 2^-18.4 of the sum
-// of |products|. An error-free sum of every product (TwoSum per product) had cost 5 us of a 30 us
+// of |products|. An error-free sum of every product (TwoSum per product) had cost 7 us of a 30 us
 // launch at the GLM size: the kernel is issue-bound there, not HBM-bound.
 #include <cuda_runtime.h>
 #include <stdint.h>
