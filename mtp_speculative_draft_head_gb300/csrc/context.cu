@@ -184,6 +184,10 @@ __global__ void __launch_bounds__(kCatWarps * 32, 4) context_concat_warps_kernel
 constexpr int kGN = 256;                  // output columns (x features) per tile
 constexpr int kGK = 64;                   // k elements per stage (one 128-byte swizzle atom)
 constexpr int kGBBytes = kGN * kGK * 2;   // 32 KB of eh_proj per stage
+#ifndef MTP_CTX_L2_AHEAD
+#define MTP_CTX_L2_AHEAD 8
+#endif
+constexpr int kCtxL2Ahead = MTP_CTX_L2_AHEAD;  // eh_proj tiles prefetched into L2 past the ring at the start
 
 // Tile of HALVES 128 x 256 FP32 accumulators (TMEM) over HALVES * 128 context rows.
 template <int HALVES>
@@ -278,12 +282,25 @@ __global__ void __launch_bounds__(Tile<HALVES>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      pdl_wait_prior_grid();  // the concat comes from the preceding kernel
       const uint64_t pol_b = l2_evict_first_policy();
       uint64_t pol_a;
       asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_a));
-      int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
+      // eh_proj does not depend on the preceding kernel (the concat): the eh_proj half of the
+      // first stages is in flight, and the next kCtxL2Ahead eh_proj tiles are on their way to L2,
+      // before the wait for it. Each stage barrier expects both halves, so a stage completes once
+      // its concat half, issued after the wait, has landed too.
+      const int pre = nkb < kGStages ? nkb : kGStages;
+      for (int kb = 0; kb < pre; ++kb) {
+        const uint32_t bar = smem_addr(&full[kb]);
+        mbar_arrive_expect_tx(bar, kGStageBytes);
+        tma_load_2d(smem_addr(smem + kb * kGStageBytes + kGABytes), &tm_b, (kb0 + kb) * kGK, n0, bar, pol_b);
+      }
+      for (int kb = pre; kb < nkb && kb < pre + kCtxL2Ahead; ++kb) tma_prefetch_l2_2d(&tm_b, (kb0 + kb) * kGK, n0);
+      pdl_wait_prior_grid();  // the concat comes from the preceding kernel
+      for (int kb = 0; kb < pre; ++kb)
+        tma_load_2d(smem_addr(smem + kb * kGStageBytes), &tm_a, (kb0 + kb) * kGK, m0, smem_addr(&full[kb]), pol_a);
+      int issued = pre;
+      for (int kb = pre; kb < nkb; ++kb) {
         const int s = kb % kGStages;
         const uint32_t ph = static_cast<uint32_t>(((kb / kGStages) & 1) ^ 1);
         if (*reinterpret_cast<volatile int*>(&abort_flag) || !mbar_wait_bounded(smem_addr(&empty[s]), ph)) {
