@@ -453,7 +453,10 @@ size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 // concat must come from HBM at least once (kHbmBytesPerUs); splitting adds the partials' write
 // and read-back and one more launch. The model only picks among correct schedules.
 CtxSched make_sched_for(int halves, int R, int H, int sm_count, double* est_us) {
-  constexpr double kCtaUs = 2.5, kHbmBytesPerUs = 6.5e6, kLaunchUs = 2.0;
+  // kSmBytesPerUs: the eh_proj bytes one CTA streams per us, about the HBM rate over all SMs (at
+  // R = 17, 96 CTAs of 48 k-blocks each took 25.5 us: 5.8 TB/s, 60 GB/s per SM); a wave of fewer
+  // CTAs than the HBM rate needs cannot reach the HBM roofline.
+  constexpr double kCtaUs = 2.5, kHbmBytesPerUs = 6.5e6, kLaunchUs = 2.0, kSmBytesPerUs = 5.0e4;
   CtxSched c{};
   c.halves = halves;
   c.tile_m = 128 * halves;
@@ -463,20 +466,31 @@ CtxSched make_sched_for(int halves, int R, int H, int sm_count, double* est_us) 
   const int T = c.mt * ((H + kGN - 1) / kGN);
   const int G = sm_count;
   const double kb_us = (halves == 2 && R > 128) ? 0.76 : 0.43;
-  const double hbm_us = (2.0 * H * 2 * H + 2.0 * R * 2 * H) / kHbmBytesPerUs;
+  // HBM floor of a wave of `ctas` CTAs over `tiles` tiles: the row tiles of one eh_proj column
+  // tile (kGN rows x 2H) read it from HBM once, the rest from L2, so a tile stands for 1 / mt of
+  // an eh_proj tile; the concat (all R rows) is read once too (cat_us)
+  const double tile_bytes = static_cast<double>(kGN) * 2 * H * 2 / c.mt;
+  auto hbm_floor = [&](double tiles, int64_t ctas) {
+    const double rate = ctas * kSmBytesPerUs < kHbmBytesPerUs ? ctas * kSmBytesPerUs : kHbmBytesPerUs;
+    return tiles * tile_bytes / rate;
+  };
+  const double cat_us = 2.0 * R * 2 * H / kHbmBytesPerUs;
   const double tile_us = c.nkb * kb_us + kCtaUs;
-  auto at_least_hbm = [&](double us) { return us > hbm_us ? us : hbm_us; };
+  auto at_least = [](double us, double floor) { return us > floor ? us : floor; };
   c.n_dp = T;
   c.n_rem = 0;
   c.splits = 1;
-  double best = at_least_hbm(static_cast<double>((T + G - 1) / G) * tile_us);
+  double best = at_least(static_cast<double>((T + G - 1) / G) * tile_us, hbm_floor(T, T < G ? T : G) + cat_us);
   const int n_dp = (T / G) * G, n_rem = T - n_dp;
   for (int sp = 2; MTP_CTX_SPLITS != 1 && n_rem > 0 && sp <= kMaxSplits && sp <= c.nkb && n_rem * sp <= kMaxSlots;
        ++sp) {
-    const int64_t waves = (static_cast<int64_t>(n_rem) * sp + G - 1) / G;
+    const int64_t rem_ctas = static_cast<int64_t>(n_rem) * sp;
+    const int64_t waves = (rem_ctas + G - 1) / G;
     const double part_bytes = static_cast<double>(n_rem) * sp * c.slot_rows * kGN * 4;
-    const double us = at_least_hbm(static_cast<double>(n_dp / G) * tile_us +
-                                   static_cast<double>(waves) * (((c.nkb + sp - 1) / sp) * kb_us + kCtaUs)) +
+    const double floor = hbm_floor(n_dp, G) + hbm_floor(n_rem, rem_ctas < G ? rem_ctas : G) + cat_us;
+    const double us = at_least(static_cast<double>(n_dp / G) * tile_us +
+                                   static_cast<double>(waves) * (((c.nkb + sp - 1) / sp) * kb_us + kCtaUs),
+                               floor) +
                       2.0 * part_bytes / kHbmBytesPerUs + kLaunchUs;
     if (us < best || (MTP_CTX_SPLITS > 1 && c.splits == 1)) {
       best = us;
