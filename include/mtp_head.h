@@ -114,11 +114,13 @@ int mtp_head_input(const uint16_t* embed, const uint16_t* enorm_w, const uint16_
  *                         case the batched input stage normalises the rows in every CTA)
  *   R              1 .. 65536 rows
  *
- * R <= 16 runs the batched input stage (one pass over eh_proj for all rows). Larger R runs two
- * kernels: the normalised concat of every row into the workspace (the same correctly rounded
- * BF16 values as the input stage), then x = concat . eh_proj^T as a tiled GEMM on the
- * tcgen05 tensor cores with FP32 accumulation -- the source's eh_proj precision, so x is the
- * BF16 rounding of an FP32-accumulated sum. H must be a multiple of 32 for R > 16
+ * With the workspace (and H a multiple of 32, R >= 2) two kernels run: the normalised concat of
+ * every row into the workspace (the same correctly rounded BF16 values as the input stage), then
+ * x = concat . eh_proj^T as a tiled GEMM on the tcgen05 tensor cores with FP32 accumulation --
+ * the source's eh_proj precision, so x is the BF16 rounding of an FP32-accumulated sum -- plus,
+ * when the GEMM splits its tiles along k, a kernel that adds their partial sums in k order.
+ * R <= 16 without the workspace (or with H not a multiple of 32, or R = 1) runs the input stage
+ * of mtp_head_input_batched instead. H must be a multiple of 32 for R > 16
  * (MTP_ERR_NOT_IMPLEMENTED otherwise).
  * ---------------------------------------------------------------------------------------- */
 int mtp_head_context_rows(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hnorm_w,
@@ -238,12 +240,13 @@ int mtp_head_logits_argmax_batched_noalloc(const uint16_t* x, const uint16_t* fi
 
 /* Bytes of workspace for the output stage and the whole-step entry points (no device query; 0
  * for invalid shapes): the output stage's part (the first 128 + 8192 * B bytes, which must be
- * zero-filled once), then room for the batched input stage's prebuilt concat (2B * H BF16 and B
- * row flags; no initialisation needed). The output stage alone accepts any workspace of at least
- * its own part. mtp_head_forward_batched / _host given a workspace of the full size build the
- * concat of B >= 6 sequences once, with one row-parallel kernel, and the tensor-core input
- * stage copies it instead of normalising it in every CTA (the same values); otherwise the input
- * stage builds it itself. */
+ * zero-filled once), then, 256-byte aligned, room for the context-row path's workspace of B rows
+ * (mtp_head_context_workspace_bytes(B, H): concat, row flags and FP32 partial sums; no
+ * initialisation needed). The output stage alone accepts any workspace of at least its own part.
+ * mtp_head_forward_batched / _host given a workspace of the full size run the input stage of
+ * 2..16 sequences at H a multiple of 32 through the context-row path (mtp_head_context_rows:
+ * concat kernel + tcgen05 GEMM; x then carries the GEMM's FP32 accumulation); otherwise they run
+ * the input stage of mtp_head_input_batched. */
 size_t mtp_head_workspace_bytes(int B, int H, int V);
 
 /* ------------------------------------------------------------------------------------------

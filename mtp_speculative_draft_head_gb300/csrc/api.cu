@@ -70,24 +70,15 @@ int validate_output(const uint16_t* x, const uint16_t* final_norm_w, const void*
 
 size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 
-// Workspace of the whole-step entry points: the output stage's part, then room for the prebuilt
-// concat of the batched input stage ([B, 2H] BF16, then [B] int32 row flags).
+// Workspace of the whole-step entry points: the output stage's part, then room for the context-row
+// path's workspace for B rows (concat, row flags, FP32 partials).
 size_t step_concat_offset(int B) { return round256(mtp::sweep_workspace_bytes(B)); }
-size_t step_workspace_bytes(int B, int H) {
-  return step_concat_offset(B) + round256(static_cast<size_t>(B) * 2 * H * 2) + round256(static_cast<size_t>(B) * 4);
-}
+size_t step_workspace_bytes(int B, int H) { return step_concat_offset(B) + mtp::context_workspace_bytes(B, H); }
 
-// cat_ws (may be null): workspace for a prebuilt concat, [B, 2H] BF16 then the [B] row flags
-// 256-byte aligned after it.
 int run_input(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hnorm_w,
               const uint16_t* eh_proj, const int32_t* tokens, const uint16_t* target_hidden,
-              uint16_t* x_out, int32_t* status, int B, int H, int V, float eps, void* stream,
-              void* cat_ws = nullptr) {
+              uint16_t* x_out, int32_t* status, int B, int H, int V, float eps, void* stream) {
   mtp::InputArgs a{};
-  if (cat_ws != nullptr) {
-    a.concat_ws = static_cast<uint16_t*>(cat_ws);
-    a.valid_ws = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(cat_ws) + round256(static_cast<size_t>(B) * 2 * H * 2));
-  }
   a.embed = embed;
   a.enorm_w = enorm_w;
   a.hnorm_w = hnorm_w;
@@ -103,6 +94,45 @@ int run_input(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hn
   a.inv_h = 1.0 / static_cast<double>(H);
   a.wait_ns = mtp::stage_wait_ns();
   return map_cuda(mtp::launch_input_stage(a, static_cast<cudaStream_t>(stream)));
+}
+
+// The context-row path into x_out: the normalised concat of every row into ws, then
+// x = concat . eh_proj^T on the tcgen05 tensor cores (FP32 accumulation), plus the in-order sum of
+// the partials of tiles split along k. H must be a multiple of 32; ws holds
+// context_workspace_bytes(R, H).
+int run_context(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hnorm_w,
+                const uint16_t* eh_proj, const int32_t* tokens, const uint16_t* target_hidden,
+                uint16_t* x_out, int32_t* status, int R, int H, int V, float eps, void* stream, void* ws) {
+  mtp::ContextArgs a{};
+  a.embed = embed;
+  a.enorm_w = enorm_w;
+  a.hnorm_w = hnorm_w;
+  a.eh_proj = eh_proj;
+  a.tokens = tokens;
+  a.hidden = target_hidden;
+  a.x = x_out;
+  a.status = status;
+  a.R = R;
+  a.H = H;
+  mtp::bind_context_workspace(&a, ws);
+  a.V = V;
+  a.eps = eps;
+  a.inv_h = 1.0 / static_cast<double>(H);
+  return map_cuda(mtp::launch_context_rows(a, static_cast<cudaStream_t>(stream)));
+}
+
+// Input stage of the whole-step entry points. With room for the context-row workspace after the
+// output stage's part (a workspace of mtp_head_workspace_bytes), 2..16 sequences at H % 32 == 0 take
+// the context-row path: its GEMM streams eh_proj from every SM and measured 26-27 us for B = 4..16
+// at H = 6144, against 36-38 us for the mma.sync kernel, whose per-stage MMA work held each CTA to
+// ~34 GB/s. ws_ctx may be null (no room): then the batched input stage runs.
+int run_step_input(const uint16_t* embed, const uint16_t* enorm_w, const uint16_t* hnorm_w,
+                   const uint16_t* eh_proj, const int32_t* tokens, const uint16_t* target_hidden,
+                   uint16_t* x_out, int32_t* status, int B, int H, int V, float eps, void* stream, void* ws_ctx) {
+  if (ws_ctx != nullptr && B >= 2 && H % 32 == 0)
+    return run_context(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidden, x_out, status, B, H, V, eps, stream,
+                       ws_ctx);
+  return run_input(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidden, x_out, status, B, H, V, eps, stream);
 }
 
 // index_base / pick: a vocabulary shard's first global row and its exchange keys (may be null).
@@ -181,8 +211,8 @@ int enqueue_host_step(const HostStep& s, const int32_t* tok, const uint16_t* hid
   void* cat = s.workspace_bytes >= step_workspace_bytes(s.B, s.H)
                   ? static_cast<uint8_t*>(s.workspace) + step_concat_offset(s.B)
                   : nullptr;
-  int v = run_input(s.embed, s.enorm_w, s.hnorm_w, s.eh_proj, s.tokens_dev, s.hidden_dev, s.x_dev, s.status, s.B,
-                    s.H, s.V, s.eps, s.stream, cat);
+  int v = run_step_input(s.embed, s.enorm_w, s.hnorm_w, s.eh_proj, s.tokens_dev, s.hidden_dev, s.x_dev, s.status,
+                         s.B, s.H, s.V, s.eps, s.stream, cat);
   if (v != MTP_OK) return v;
   v = run_output(s.x_dev, s.final_norm_w, s.lm_head, s.row_scale, s.w_dtype, nullptr, s.draft_dev, s.status,
                  s.workspace, s.B, s.H, s.V, s.eps, s.stream);
@@ -249,8 +279,8 @@ std::shared_ptr<StepGraph> record_step(const HostStep& s, int device) {
       void* cat = s.workspace_bytes >= step_workspace_bytes(s.B, s.H)
                       ? static_cast<uint8_t*>(s.workspace) + step_concat_offset(s.B)
                       : nullptr;
-      v = run_input(s.embed, s.enorm_w, s.hnorm_w, s.eh_proj, s.tokens_dev, s.hidden_dev, s.x_dev, s.status, s.B,
-                    s.H, s.V, s.eps, s.stream, cat);
+      v = run_step_input(s.embed, s.enorm_w, s.hnorm_w, s.eh_proj, s.tokens_dev, s.hidden_dev, s.x_dev, s.status,
+                         s.B, s.H, s.V, s.eps, s.stream, cat);
     }
     if (v == MTP_OK)
       v = run_output(s.x_dev, s.final_norm_w, s.lm_head, s.row_scale, s.w_dtype, nullptr, s.draft_dev, s.status,
@@ -424,11 +454,10 @@ int mtp_head_forward_batched(const uint16_t* embed, const uint16_t* enorm_w,
   v = validate_output(x, final_norm_w, lm_head, row_scale, w_dtype, logits, draft, status, workspace,
                       workspace_bytes, B, H, V, eps);
   if (v != MTP_OK) return v;
-  // a workspace of the full size also takes the prebuilt concat of the batched input stage
+  // a workspace of the full size also holds the context-row path's workspace
   void* cat = workspace_bytes >= step_workspace_bytes(B, H) ? static_cast<uint8_t*>(workspace) + step_concat_offset(B)
                                                              : nullptr;
-  v = run_input(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidden, x, status, B, H, V, eps,
-                stream, cat);
+  v = run_step_input(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidden, x, status, B, H, V, eps, stream, cat);
   if (v != MTP_OK) return v;
   return run_output(x, final_norm_w, lm_head, row_scale, w_dtype, logits, draft, status, workspace,
                     B, H, V, eps, stream);
@@ -470,30 +499,13 @@ int mtp_head_context_rows(const uint16_t* embed, const uint16_t* enorm_w, const 
       !aligned(target_hidden, 16) || !aligned(x_out, 16) || !aligned(tokens, 4) ||
       (status && !aligned(status, 4)) || (workspace && !aligned(workspace, 16)))
     return MTP_ERR_ALIGN;
-  if (R <= kMaxB) {  // a few rows: the batched input stage, one weight pass for all of them
-    // its concat and row flags sit where this entry point's own kernels put them
-    void* cat = (workspace && workspace_bytes >= mtp::context_workspace_bytes(R, H)) ? workspace : nullptr;
-    return run_input(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidden, x_out, status, R, H, V, eps,
-                     stream, cat);
-  }
+  const bool have_ws = workspace && workspace_bytes >= mtp::context_workspace_bytes(R, H);
+  if (R <= kMaxB && (!have_ws || R == 1 || H % 32 != 0))  // a few rows without room: the batched input stage
+    return run_input(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidden, x_out, status, R, H, V, eps, stream);
   if (H % 32 != 0) return MTP_ERR_NOT_IMPLEMENTED;
-  if (!workspace || workspace_bytes < mtp::context_workspace_bytes(R, H)) return MTP_ERR_WORKSPACE;
-  mtp::ContextArgs a{};
-  a.embed = embed;
-  a.enorm_w = enorm_w;
-  a.hnorm_w = hnorm_w;
-  a.eh_proj = eh_proj;
-  a.tokens = tokens;
-  a.hidden = target_hidden;
-  a.x = x_out;
-  a.status = status;
-  a.R = R;
-  a.H = H;
-  mtp::bind_context_workspace(&a, workspace);
-  a.V = V;
-  a.eps = eps;
-  a.inv_h = 1.0 / static_cast<double>(H);
-  return map_cuda(mtp::launch_context_rows(a, static_cast<cudaStream_t>(stream)));
+  if (!have_ws) return MTP_ERR_WORKSPACE;
+  return run_context(embed, enorm_w, hnorm_w, eh_proj, tokens, target_hidden, x_out, status, R, H, V, eps, stream,
+                     workspace);
 }
 
 int mtp_head_quantize_fp8(const uint16_t* w, uint8_t* q, float* row_scale, int32_t* status, int V,

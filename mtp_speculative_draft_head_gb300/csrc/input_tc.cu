@@ -71,9 +71,6 @@ constexpr int kPrologueThreads = (kCW + kBW) * 32;
 #ifndef MTP_IN_FENCE
 #define MTP_IN_FENCE 1
 #endif
-#ifndef MTP_IN_PRECAT
-#define MTP_IN_PRECAT 6  // smallest batch that uses a caller workspace, when given, for a prebuilt concat
-#endif
 constexpr int kCK = MTP_IN_CK;                // k elements per stage
 constexpr int kPitch = kCK * 2 + 16;          // padded row bytes in shared memory
 constexpr int kWStageBytes = 8 * kCK * 2;     // one n-tile: 8 weight rows x kCK, 128B-swizzled
@@ -125,7 +122,6 @@ __global__ void __launch_bounds__(kInTcThreads, 1)
   const int nrows = 8 * (g1 - g0);
   const int ntiles = g1 - g0;
   const int nck = (K + kCK - 1) / kCK;
-  const bool pre = a.concat != nullptr;  // the concat was built once, before this kernel
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWStages; ++i) {
@@ -163,7 +159,6 @@ __global__ void __launch_bounds__(kInTcThreads, 1)
         const uint32_t hoff = static_cast<uint32_t>(h0 - k0) * 2;
         uint32_t bytes = eb + hb;  // the norm-weight segment
         for (int b = 0; b < B; ++b) bytes += (valid_s[b] ? eb : 0u) + hb;
-        if (pre) bytes = static_cast<uint32_t>(B) * static_cast<uint32_t>(k1 - k0) * 2;
         if (*reinterpret_cast<volatile int*>(&abort_flag) || !mbar_wait_bounded(smem_addr(&aempty[slot]), ep)) {
           ok = false;
           break;
@@ -171,18 +166,12 @@ __global__ void __launch_bounds__(kInTcThreads, 1)
         const uint32_t bar = smem_addr(&xfull[slot]);
         const uint32_t dst = smem_addr(aring + slot * kAStageBytes);
         mbar_arrive_expect_tx(bar, bytes);
-        if (pre) {  // the chunk of every prebuilt concat row, already normalised
-          for (int b = 0; b < B; ++b)
-            bulk_copy_g2s(dst + b * kPitch, a.concat + static_cast<size_t>(b) * K + k0,
-                          static_cast<uint32_t>(k1 - k0) * 2, bar, policy);
-        } else {
-          if (eb) bulk_copy_g2s(dst + kAWOffset, a.enorm_w + k0, eb, bar, policy);
-          if (hb) bulk_copy_g2s(dst + kAWOffset + hoff, a.hnorm_w + (h0 - H), hb, bar, policy);
-          for (int b = 0; b < B; ++b) {
-            if (eb && valid_s[b])
-              bulk_copy_g2s(dst + b * kPitch, a.embed + static_cast<int64_t>(tok_s[b]) * H + k0, eb, bar, policy);
-            if (hb) bulk_copy_g2s(dst + b * kPitch + hoff, a.hidden + static_cast<size_t>(b) * H + (h0 - H), hb, bar, policy);
-          }
+        if (eb) bulk_copy_g2s(dst + kAWOffset, a.enorm_w + k0, eb, bar, policy);
+        if (hb) bulk_copy_g2s(dst + kAWOffset + hoff, a.hnorm_w + (h0 - H), hb, bar, policy);
+        for (int b = 0; b < B; ++b) {
+          if (eb && valid_s[b])
+            bulk_copy_g2s(dst + b * kPitch, a.embed + static_cast<int64_t>(tok_s[b]) * H + k0, eb, bar, policy);
+          if (hb) bulk_copy_g2s(dst + b * kPitch + hoff, a.hidden + static_cast<size_t>(b) * H + (h0 - H), hb, bar, policy);
         }
         ++issued;
         if (++slot == kAStages) { slot = 0; ep ^= 1u; }
@@ -201,12 +190,7 @@ __global__ void __launch_bounds__(kInTcThreads, 1)
     // ------------------------------------------------------------------ weight producer
     // Both streams start once the prologue has read the embedding rows and target_hidden:
     // issued first, ~20 MB of loads over all SMs sit in front of those in the memory queues.
-    // With a prebuilt concat the prologue reads only the tokens, so the weights start at once
-    // (eh_proj does not depend on the preceding kernels).
-    if (pre)
-      asm volatile("bar.arrive %0, %1;" ::"r"(kBarInRead), "r"(kPrologueThreads + 64) : "memory");
-    else
-      asm volatile("bar.sync %0, %1;" ::"r"(kBarInRead), "r"(kPrologueThreads + 64) : "memory");
+    asm volatile("bar.sync %0, %1;" ::"r"(kBarInRead), "r"(kPrologueThreads + 64) : "memory");
     if (lane == 0) {
       const uint64_t policy = l2_evict_first_policy();
       int slot = 0, issued = 0;
@@ -254,9 +238,9 @@ __global__ void __launch_bounds__(kInTcThreads, 1)
         if (j & 1) return a.hidden + static_cast<size_t>(b) * H;
         return valid_s[b] ? a.embed + static_cast<int64_t>(tok_s[b]) * H : nullptr;
       };
-      if (!pre) sumsq_rows<kPrologueThreads, 8, false>(2 * B, H, row, nullptr, part, nullptr, tot, nullptr, 1);
+      sumsq_rows<kPrologueThreads, 8, false>(2 * B, H, row, nullptr, part, nullptr, tot, nullptr, 1);
       asm volatile("bar.arrive %0, %1;" ::"r"(kBarInRead), "r"(kPrologueThreads + 64) : "memory");
-      if (!pre && threadIdx.x < 2 * B) {
+      if (threadIdx.x < 2 * B) {
         const int b = threadIdx.x >> 1, half = threadIdx.x & 1;
         const DF t = tot[threadIdx.x];
         // 1 / rms in fp64 (rsqrt: within an ulp or two of the correctly rounded value)
@@ -291,7 +275,7 @@ __global__ void __launch_bounds__(kInTcThreads, 1)
           break;
         }
         uint8_t* base = aring + slot * kAStageBytes;
-        for (int cell = bt; !pre && cell < B * kCells; cell += kBW * 32) {
+        for (int cell = bt; cell < B * kCells; cell += kBW * 32) {
           const int b = cell / kCells, c = cell - b * kCells;
           if (c < ppr) {
             const int half = k0 + 8 * c >= H ? 1 : 0;
@@ -456,30 +440,6 @@ cudaError_t launch_input_tc(const InputArgs& a, cudaStream_t stream, bool* launc
   if (per > kMaxTiles) per = kMaxTiles;
   grid = (ngroups + per - 1) / per;
   InputArgs args = a;
-  args.concat = nullptr;
-  // the prebuilt concat pays from about six sequences on (measured at H = 6144: B = 8 and 16
-  // gain 4 and 24 us; B = 2 and 4 lose 4 and 1 us to the extra kernel on the critical path)
-  if (a.concat_ws != nullptr && a.valid_ws != nullptr && a.B >= MTP_IN_PRECAT) {
-    ContextArgs c{};
-    c.embed = a.embed;
-    c.enorm_w = a.enorm_w;
-    c.hnorm_w = a.hnorm_w;
-    c.eh_proj = a.eh_proj;
-    c.tokens = a.tokens;
-    c.hidden = a.hidden;
-    c.x = a.x;
-    c.status = a.status;
-    c.concat = a.concat_ws;
-    c.valid = a.valid_ws;
-    c.R = a.B;
-    c.H = a.H;
-    c.V = a.V;
-    c.eps = a.eps;
-    c.inv_h = a.inv_h;
-    err = launch_context_concat(c, stream);
-    if (err != cudaSuccess) return err;
-    args.concat = a.concat_ws;
-  }
   CUtensorMap tmc = tm;
   void* params[] = {&tmc, &args};
   *launched = true;

@@ -77,12 +77,6 @@ struct InputArgs {
   double inv_h;  // 1 / H (fp64), for the mean of squares
   int stages;  // pipeline stages (bulk-copy kernel)
   int group;   // sequences whose concat is resident at once (plain kernel)
-  // Optional caller workspace for a prebuilt concat ([B, 2H] BF16, then [B] int32 row flags):
-  // when given, the tensor-core kernel's launcher builds the concat there once (the row-parallel
-  // concat kernel) and the kernel copies it instead of normalising it in every CTA.
-  uint16_t* concat_ws;
-  int32_t* valid_ws;
-  const uint16_t* concat;  // set by that launcher: the prebuilt concat the kernel reads
   unsigned long long wait_ns;  // give-up time of the single-sequence kernel's stage waits
 };
 

@@ -45,10 +45,29 @@ def single_x_band(H: int) -> float:
 
 
 def x_band(H: int, B: int) -> float:
-    """The accumulation band of x for B sequences: the single-sequence kernel at B = 1; the
-    tensor-core kernel (or, for shapes it does not take, the CUDA-core kernels) at B >= 2."""
+    """The accumulation band of x from mtp_head_input_batched (no workspace) for B sequences:
+    the single-sequence kernel at B = 1; the tensor-core kernel (or, for shapes it does not take,
+    the CUDA-core kernels) at B >= 2."""
     single = single_x_band(H)
     return single if B == 1 else max(BATCHED_X_BAND, single)
+
+
+def context_band(K: int) -> float:
+    """Relative band (times sum_k |p_k|) of an FP32 accumulation of K exact BF16 products on the
+    tcgen05 tensor cores (the context-row GEMM): the MMAs add K / 16 groups of 16 exact products
+    into FP32 accumulators, and each of those additions (with whatever internal alignment the
+    hardware uses inside a group) is taken to err by at most 2^-22 of the sum of |products|
+    accumulated so far. When the product is split along k, the at most 15 FP32 additions of the
+    split partial sums (round to nearest, each within 2^-24 of a value bounded by the sum of
+    |products|) fit in the extra 16 * 2^-22."""
+    return (K / 16 + 16) * 2.0 ** -22
+
+
+def step_x_band(H: int, B: int) -> float:
+    """The band of x from the whole-step entry points with a workspace of the full
+    mtp_head_workspace_bytes: 2..16 sequences at H % 32 == 0 take the context-row GEMM, the rest
+    the kernels of mtp_head_input_batched."""
+    return context_band(2 * H) if B >= 2 and H % 32 == 0 else x_band(H, B)
 
 
 def abs_product_sums(eh_proj_bits: np.ndarray, concat_bits: np.ndarray) -> np.ndarray:

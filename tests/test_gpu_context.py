@@ -13,23 +13,12 @@ import torch
 import mtp_speculative_draft_head_gb300 as m
 import oracle
 import synth
-from gpu_helpers import abs_product_sums, check_x
+from gpu_helpers import abs_product_sums, check_x, context_band
 
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
 EPS = synth.EPS
-
-
-def context_band(K: int) -> float:
-    """Relative band (times sum_k |p_k|) of an FP32 accumulation of K exact BF16 products on the
-    tensor cores: the MMAs add K / 16 groups of 16 exact products into FP32 accumulators, and
-    each of those additions (with whatever internal alignment the hardware uses inside a group)
-    is taken to err by at most 2^-22 of the sum of |products| accumulated so far. When the
-    product is split along k, the at most 15 FP32 additions of the split partial sums (round to
-    nearest, each within 2^-24 of a value bounded by the sum of |products|) fit in the extra
-    16 * 2^-22."""
-    return (K / 16 + 16) * 2.0 ** -22
 
 
 class Ctx:
@@ -143,19 +132,26 @@ def test_context_rows_out_of_range_tokens(H, R):
     check_rows(c, x, ws)
 
 
-def test_context_rows_small_r_is_batched_input():
-    """R <= 16 runs the batched input stage: identical to mtp_head_input_batched, no workspace."""
-    H, R = 1024, 9
-    c = Ctx(H, R, seed=5)
-    x, st, _ = c.run()
+@pytest.mark.parametrize("R", [2, 9, 16])
+def test_context_rows_small_r(R):
+    """R <= 16: with a workspace (H a multiple of 32) the context-row path, checked like every R;
+    without one, the batched input stage, identical to mtp_head_input_batched."""
+    H = 1024
+    c = Ctx(H, R, seed=5 + R)
+    x, st, ws = c.run()
     assert st == 0
-    x = synth.bits(x)
+    check_rows(c, x, ws)
+    xn = torch.full((R, H), 7, dtype=torch.bfloat16, device=DEV)
+    stn = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.mtp_head_context_rows(c.g["embed"], c.g["enorm_w"], c.g["hnorm_w"], c.g["eh_proj"], c.tokens.to(DEV),
+                            c.hidden.to(DEV), xn, None, stn, EPS)
     xb = torch.full((R, H), 7, dtype=torch.bfloat16, device=DEV)
     stb = torch.zeros(1, dtype=torch.int32, device=DEV)
     m.mtp_head_input_batched(c.g["embed"], c.g["enorm_w"], c.g["hnorm_w"], c.g["eh_proj"], c.tokens.to(DEV),
                              c.hidden.to(DEV), xb, stb, EPS)
     torch.cuda.synchronize()
-    assert np.array_equal(x, synth.bits(xb))
+    assert int(stn.item()) == 0 and int(stb.item()) == 0
+    assert np.array_equal(synth.bits(xn), synth.bits(xb))
 
 
 def test_context_rows_deterministic_and_workspace_checked():

@@ -11,7 +11,8 @@ import torch
 import mtp_speculative_draft_head_gb300 as m
 import oracle
 import synth
-from gpu_helpers import TOL_BF16, TOL_FP8, abs_product_sums, check_draft, check_logits_and_draft, check_x, x_band
+from gpu_helpers import (TOL_BF16, TOL_FP8, abs_product_sums, check_draft, check_logits_and_draft, check_x, step_x_band,
+                         x_band)
 
 pytestmark = pytest.mark.gpu
 
@@ -82,7 +83,7 @@ def test_glm_head(glm, B, fp8):
     assert int(status.item()) == 0
     x_ref, st, sums, abs_sums = glm.oracle_x(tokens, hidden)
     assert np.all(st == 0)
-    n_diff = check_x(_bits(x), x_ref, sums, abs_sums, x_band(glm.H, B))
+    n_diff = check_x(_bits(x), x_ref, sums, abs_sums, step_x_band(glm.H, B))
     # the band is a worst-case bound; the FP32 runs differ from the exact sum far more rarely
     assert n_diff <= max(1, x_ref.size // 100)
     ref = glm.oracle_logits(x_ref, fp8)

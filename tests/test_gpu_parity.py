@@ -13,6 +13,7 @@ import mtp_speculative_draft_head_gb300 as m
 import oracle
 import synth
 from gpu_helpers import (TOL_BF16, TOL_FP8, abs_product_sums, check_draft, check_logits_and_draft, check_x, x_band,
+                         step_x_band,
                          lowest_argmax)
 
 pytestmark = pytest.mark.gpu
@@ -132,7 +133,9 @@ def test_head_matches_oracle(H, V, B, fp8):
     # ... without storing logits (same draft) ...
     _, draft3, _ = c.output_gpu(x_gpu, W, scale, wt, want_logits=False)
     assert torch.equal(draft3, draft)
-    # ... and through the one-call forward (bitwise the same)
+    # ... and through the one-call forward: with the full-size workspace its input stage takes
+    # the context-row GEMM for 2..16 sequences at H % 32 == 0 (checked against its own band), else
+    # the kernels above (bitwise the same); its output stage is the one above, bit for bit
     xf = torch.empty_like(x_gpu)
     lf = torch.empty_like(logits)
     df = torch.empty_like(draft)
@@ -140,8 +143,14 @@ def test_head_matches_oracle(H, V, B, fp8):
                                c.g["final_norm_w"], W, scale, wt, c.tokens.to(DEV), c.hidden.to(DEV),
                                xf, lf, df, c.ws, None, EPS)
     torch.cuda.synchronize()
-    assert torch.equal(xf, x_gpu) and torch.equal(df, draft)
-    assert torch.equal(lf.view(torch.int32), logits.view(torch.int32))
+    if B >= 2 and H % 32 == 0:
+        n_diff = check_x(_bits(xf), x_ref, sums, c.abs_sums(), step_x_band(H, B))
+        assert n_diff <= max(1, x_ref.size // 100)
+        lo, do, _ = c.output_gpu(xf, W, scale, wt)
+        assert torch.equal(df, do) and torch.equal(lf.view(torch.int32), lo.view(torch.int32))
+    else:
+        assert torch.equal(xf, x_gpu) and torch.equal(df, draft)
+        assert torch.equal(lf.view(torch.int32), logits.view(torch.int32))
 
 
 def test_worked_example_on_gpu(golden_dir):
@@ -266,7 +275,13 @@ def test_planted_ties_lowest_index_wins(fp8):
 
 def test_repeat_calls_are_bitwise_identical_and_graph_replay_matches():
     c = Case(2048, 30000, 2, seed=10)
-    x, _ = c.input_gpu()
+    # x of the whole step (its input stage is the context-row GEMM here), eagerly
+    x = torch.empty((2, c.H), dtype=torch.bfloat16, device=DEV)
+    d0 = torch.empty(2, dtype=torch.int32, device=DEV)
+    m.mtp_head_forward_batched(c.g["embed"], c.g["enorm_w"], c.g["hnorm_w"], c.g["eh_proj"], c.g["final_norm_w"],
+                               c.g["lm_head"], None, m.W_BF16, c.tokens.to(DEV), c.hidden.to(DEV), x, None, d0,
+                               c.ws, None, EPS)
+    torch.cuda.synchronize()
     outs = [c.output_gpu(x, c.g["lm_head"], None, m.W_BF16) for _ in range(3)]
     for lg, dr, _ in outs[1:]:
         assert torch.equal(lg.view(torch.int32), outs[0][0].view(torch.int32)) and torch.equal(dr, outs[0][1])
@@ -497,18 +512,19 @@ def test_fp8_every_code_including_subnormals(H):
 
 
 @pytest.mark.parametrize("H,B", [(6144, 16), (1024, 6), (2048, 8), (96, 9), (1024, 2)])
-def test_prebuilt_concat_gives_the_same_x(H, B):
-    """With a full-size workspace and B >= 6 the whole-step entry point builds the batch's concat
-    once (row kernel) and the tensor-core input stage copies it; without one,
-    mtp_head_input_batched normalises in every CTA (as the whole step does for B < 6). Same
-    arithmetic, so x must be identical bit for bit -- including the zero row of an out-of-range
-    token -- and the status the same."""
+def test_whole_step_input_is_the_context_row_path(H, B):
+    """With a full-size workspace, the whole-step entry point runs 2..16 sequences at H % 32 == 0
+    through the context-row path (concat kernel + tcgen05 GEMM): its x must equal
+    mtp_head_context_rows's bit for bit -- including the zero row of an out-of-range token -- with
+    the same status, and lie within that path's band of the oracle."""
     c = Case(H, 700, B, seed=H + 3 * B)
     tokens = c.tokens.clone()
     tokens[B // 2] = c.V + 5
-    x_in, st_in = c.input_gpu(tokens=tokens)
-    assert st_in == m.ERR_TOKEN_RANGE
     assert c.ws.numel() >= m.mtp_head_workspace_bytes(B, H, c.V)
+    x_cr = torch.full((B, H), 7, dtype=torch.bfloat16, device=DEV)
+    st_cr = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.mtp_head_context_rows(c.g["embed"], c.g["enorm_w"], c.g["hnorm_w"], c.g["eh_proj"], tokens.to(DEV),
+                            c.hidden.to(DEV), x_cr, m.context_workspace(B, H, DEV), st_cr, EPS)
     x_fw = torch.full((B, H), 7, dtype=torch.bfloat16, device=DEV)
     d = torch.empty(B, dtype=torch.int32, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
@@ -516,9 +532,14 @@ def test_prebuilt_concat_gives_the_same_x(H, B):
                                c.g["lm_head"], None, m.W_BF16, tokens.to(DEV), c.hidden.to(DEV), x_fw, None, d,
                                c.ws, st, EPS)
     torch.cuda.synchronize()
-    assert int(st.item()) == m.ERR_TOKEN_RANGE
-    assert torch.equal(x_fw.view(torch.int16), x_in.view(torch.int16))
+    assert int(st.item()) == m.ERR_TOKEN_RANGE and int(st_cr.item()) == m.ERR_TOKEN_RANGE
+    assert torch.equal(x_fw.view(torch.int16), x_cr.view(torch.int16))
     assert bool((x_fw[B // 2].view(torch.int16) == 0).all())
+    x_ref, concat, _, sums = oracle.input_stage(c.wb["embed"], c.wb["enorm_w"], c.wb["hnorm_w"], c.wb["eh_proj"],
+                                                _bits(tokens).astype(np.int64), _bits(c.hidden), EPS,
+                                                return_concat=True, return_sums=True)
+    n_diff = check_x(_bits(x_fw), x_ref, sums, abs_product_sums(c.wb["eh_proj"], concat), step_x_band(H, B))
+    assert n_diff <= max(1, x_ref.size // 100)
 
 
 @pytest.mark.parametrize("H,B", [(256, 3), (100, 1)])  # moves as kernels; B * H % 8 != 0: copy operations
