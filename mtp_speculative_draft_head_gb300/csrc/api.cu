@@ -234,6 +234,9 @@ struct StepGraph {
   uint16_t* hid = nullptr;
   int32_t* draft = nullptr;
   int32_t* st = nullptr;
+  uint32_t* seq = nullptr;    // [0] this call's number, [1] the number the last kernel wrote when done
+  uint32_t calls = 0;
+  bool polled = false;        // the graph ends in the kernel that writes seq[1]
   uint64_t last_use = 0;
   ~StepGraph() {
     if (exec) cudaGraphExecDestroy(exec);
@@ -262,6 +265,8 @@ std::shared_ptr<StepGraph> record_step(const HostStep& s, int device) {
   g->tok = reinterpret_cast<int32_t*>(base);
   g->draft = reinterpret_cast<int32_t*>(base + tok_bytes);
   g->st = reinterpret_cast<int32_t*>(base + 2 * tok_bytes);
+  g->seq = reinterpret_cast<uint32_t*>(base + 2 * tok_bytes + 8);
+  g->seq[0] = g->seq[1] = 0u;
   g->hid = reinterpret_cast<uint16_t*>(base + 2 * tok_bytes + 16);
   // the device's view of the staging buffers: the moves in and out are kernels reading and
   // writing them directly (whole 16-byte pieces of hidden rows); otherwise copy operations
@@ -287,7 +292,9 @@ std::shared_ptr<StepGraph> record_step(const HostStep& s, int device) {
                      s.workspace, s.B, s.H, s.V, s.eps, s.stream);
     if (v == MTP_OK)
       v = map_cuda(mtp::launch_host_out(s.draft_dev, reinterpret_cast<int32_t*>(dbase + tok_bytes), s.status,
-                                        reinterpret_cast<int32_t*>(dbase + 2 * tok_bytes), s.B, s.stream));
+                                        reinterpret_cast<int32_t*>(dbase + 2 * tok_bytes), s.B,
+                                        reinterpret_cast<const uint32_t*>(dbase + 2 * tok_bytes + 8),
+                                        reinterpret_cast<uint32_t*>(dbase + 2 * tok_bytes + 12), s.stream));
   } else {
     v = enqueue_host_step(s, g->tok, g->hid, g->draft, g->st);
   }
@@ -305,7 +312,23 @@ std::shared_ptr<StepGraph> record_step(const HostStep& s, int device) {
     cudaGetLastError();
     return nullptr;
   }
+  g->polled = kernel_io;
   return g;
+}
+
+// Waits for a recorded step that ends in the kernel writing the completion word: polls the word
+// (the draft and status are visible once it holds this call's number), and every 4096 polls asks
+// the stream, so that a failed launch returns its error and a finished stream ends the wait. This
+// avoids the wake-up latency of a stream synchronisation, a few microseconds per step.
+int wait_step(const uint32_t* done_word, uint32_t n, cudaStream_t stream) {
+  for (uint64_t i = 1;; ++i) {
+    if (__atomic_load_n(done_word, __ATOMIC_ACQUIRE) == n) return MTP_OK;
+    if ((i & 4095u) == 0) {
+      const cudaError_t q = cudaStreamQuery(stream);
+      if (q == cudaSuccess) return __atomic_load_n(done_word, __ATOMIC_ACQUIRE) == n ? MTP_OK : MTP_ERR_CUDA;
+      if (q != cudaErrorNotReady) return MTP_ERR_CUDA;
+    }
+  }
 }
 
 int run_host_step(const HostStep& s, const int32_t* tokens_host, const uint16_t* hidden_host, int32_t* draft_host) {
@@ -350,8 +373,19 @@ int run_host_step(const HostStep& s, const int32_t* tokens_host, const uint16_t*
   memcpy(g->tok, tokens_host, sizeof(int32_t) * s.B);
   memcpy(g->hid, hidden_host, sizeof(uint16_t) * static_cast<size_t>(s.B) * s.H);
   *g->st = 0;
+  uint32_t n = 0;
+  if (g->polled) {
+    n = ++g->calls;
+    if (n == 0) n = ++g->calls;  // 0 is the word's initial value
+    __atomic_store_n(&g->seq[0], n, __ATOMIC_RELEASE);
+  }
   if (cudaGraphLaunch(g->exec, s.stream) != cudaSuccess) return MTP_ERR_CUDA;
-  if (cudaStreamSynchronize(s.stream) != cudaSuccess) return MTP_ERR_CUDA;
+  if (g->polled) {
+    const int v = wait_step(&g->seq[1], n, s.stream);
+    if (v != MTP_OK) return v;
+  } else if (cudaStreamSynchronize(s.stream) != cudaSuccess) {
+    return MTP_ERR_CUDA;
+  }
   memcpy(draft_host, g->draft, sizeof(int32_t) * s.B);
   return s.status ? *g->st : MTP_OK;
 }

@@ -35,12 +35,19 @@ __global__ void __launch_bounds__(kIoThreads) host_in_kernel(const int32_t* __re
   if (blockIdx.x == 0 && threadIdx.x < B) tok_dst[threadIdx.x] = tok_src[threadIdx.x];
 }
 
+// One thread writes the drafts and the status into host memory, makes them visible to the host
+// (system-scope fence), then copies the call's sequence number (seq_in, set by the host before
+// the launch) to seq_out, which the host polls instead of waiting for the stream (may be null).
 __global__ void __launch_bounds__(32) host_out_kernel(const int32_t* draft_src, int32_t* draft_dst,
-                                                      const int32_t* status_src, int32_t* status_dst, int B) {
+                                                      const int32_t* status_src, int32_t* status_dst, int B,
+                                                      const uint32_t* seq_in, uint32_t* seq_out) {
   pdl_wait_prior_grid();  // the draft comes from the sweep
-  if (threadIdx.x < B) draft_dst[threadIdx.x] = draft_src[threadIdx.x];
-  if (threadIdx.x == 0 && status_src != nullptr) *status_dst = *status_src;
-  __threadfence_system();
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < B; ++b) draft_dst[b] = draft_src[b];
+    if (status_src != nullptr) *status_dst = *status_src;
+    __threadfence_system();
+    if (seq_out != nullptr) *reinterpret_cast<volatile uint32_t*>(seq_out) = *reinterpret_cast<const volatile uint32_t*>(seq_in);
+  }
 }
 
 }  // namespace
@@ -60,11 +67,11 @@ cudaError_t launch_host_in(const int32_t* tok_src, const uint16_t* hid_src, int3
 }
 
 cudaError_t launch_host_out(const int32_t* draft_src, int32_t* draft_dst, const int32_t* status_src, int32_t* status_dst,
-                            int B, cudaStream_t stream) {
+                            int B, const uint32_t* seq_in, uint32_t* seq_out, cudaStream_t stream) {
   DeviceInfo di;
   cudaError_t err = device_info(&di);
   if (err != cudaSuccess) return err;
-  void* params[] = {&draft_src, &draft_dst, &status_src, &status_dst, &B};
+  void* params[] = {&draft_src, &draft_dst, &status_src, &status_dst, &B, &seq_in, &seq_out};
   return launch_pdl(reinterpret_cast<const void*>(host_out_kernel), dim3(1), dim3(32), 0, stream, params);
 }
 

@@ -137,11 +137,12 @@ cudaError_t launch_sweep(const SweepArgs& a, cudaStream_t stream);
 // not supported (H not a multiple of 8, no tensor-map encoder, not enough shared memory).
 cudaError_t launch_sweep_tc(const SweepArgs& a, cudaStream_t stream, bool* launched);
 // The host-buffer step's moves as kernels on mapped pinned memory (device addresses of host
-// buffers): hidden [B, H] (B * H a multiple of 8) and tokens in; draft and status (may be null) out.
+// buffers): hidden [B, H] (B * H a multiple of 8) and tokens in; draft and status (may be null) out,
+// then the completion word seq_out set to *seq_in (both may be null).
 cudaError_t launch_host_in(const int32_t* tok_src, const uint16_t* hid_src, int32_t* tok_dst, uint16_t* hid_dst,
                            int B, int H, cudaStream_t stream);
 cudaError_t launch_host_out(const int32_t* draft_src, int32_t* draft_dst, const int32_t* status_src, int32_t* status_dst,
-                            int B, cudaStream_t stream);
+                            int B, const uint32_t* seq_in, uint32_t* seq_out, cudaStream_t stream);
 cudaError_t launch_quantize(const uint16_t* w, uint8_t* q, float* scale, int32_t* status,
                             int V, int H, cudaStream_t stream);
 // Pick over R shards' exchange keys picks[r * B + b]: draft[b] (global index, -1 if empty) and
