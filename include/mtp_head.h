@@ -279,7 +279,11 @@ int mtp_head_forward_batched(const uint16_t* embed, const uint16_t* enorm_w,
  * moves between the staging buffers and tokens_dev / hidden_dev / draft_dev are small kernels
  * on the mapped memory (when B * H is a multiple of 8; copy operations otherwise). The host buffers may
  * differ from call to call. Calls from several threads are safe; calls sharing a recorded
- * step are serialised.
+ * step are serialised. On that recorded path the call returns as soon as the step's last kernel
+ * has written the draft and status to the staging memory and set a completion word there (the
+ * host polls it, asking the stream now and then so that a failed launch returns MTP_ERR_CUDA),
+ * which spares the wake-up of a stream synchronisation; the stream may then still be retiring
+ * that kernel, so work on another stream that must follow this step should wait on `stream`.
  * ---------------------------------------------------------------------------------------- */
 int mtp_head_forward_host(const uint16_t* embed, const uint16_t* enorm_w,
                           const uint16_t* hnorm_w, const uint16_t* eh_proj,
