@@ -53,8 +53,12 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sweep_traffic.json")
+# what the single-sequence sweep kernels are built from: their source, the device helpers they
+# include, and the part of the internal header up to their argument struct (tuning constants,
+# SweepArgs); the host declarations after it do not change them
 SWEEP_SOURCES = [os.path.join(ROOT, "mtp_speculative_draft_head_gb300", "csrc", f)
-                 for f in ("sweep.cu", "common.cuh", "internal.h")]
+                 for f in ("sweep.cu", "common.cuh", "pick.h")]
+SWEEP_HEADER = os.path.join(ROOT, "mtp_speculative_draft_head_gb300", "csrc", "internal.h")
 
 
 # ------------------------------------------------------------------ algorithmic bytes
@@ -186,6 +190,9 @@ def sweep_source_sha() -> str:
     for p in SWEEP_SOURCES:
         with open(p, "rb") as f:
             h.update(f.read())
+    with open(SWEEP_HEADER, "rb") as f:
+        text = f.read()
+    h.update(text[:text.index(b"struct ContextArgs")])
     return h.hexdigest()[:16]
 
 

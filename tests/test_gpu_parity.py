@@ -542,6 +542,23 @@ def test_whole_step_input_is_the_context_row_path(H, B):
     assert n_diff <= max(1, x_ref.size // 100)
 
 
+@pytest.mark.parametrize("H,B", [(520, 3), (1000, 16), (2056, 2)])
+def test_whole_step_input_without_the_gemm_shape(H, B):
+    """H not a multiple of 32: the whole-step entry point runs the kernels of
+    mtp_head_input_batched even with a full-size workspace, so x is theirs bit for bit."""
+    c = Case(H, 900, B, seed=H + B)
+    x_in, st_in = c.input_gpu()
+    x_fw = torch.full((B, H), 7, dtype=torch.bfloat16, device=DEV)
+    d = torch.empty(B, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.mtp_head_forward_batched(c.g["embed"], c.g["enorm_w"], c.g["hnorm_w"], c.g["eh_proj"], c.g["final_norm_w"],
+                               c.g["lm_head"], None, m.W_BF16, c.tokens.to(DEV), c.hidden.to(DEV), x_fw, None, d,
+                               c.ws, st, EPS)
+    torch.cuda.synchronize()
+    assert st_in == 0 and int(st.item()) == 0
+    assert torch.equal(x_fw.view(torch.int16), x_in.view(torch.int16))
+
+
 @pytest.mark.parametrize("H,B", [(256, 3), (100, 1)])  # moves as kernels; B * H % 8 != 0: copy operations
 @pytest.mark.parametrize("fp8", [False, True])
 def test_host_forward_graph_replays_match_device_path(fp8, H, B):
