@@ -256,3 +256,16 @@ def test_pick_key_empty(lib):
     assert m.mtp_head_pick_index(empty) == -1
     assert m.mtp_head_pick_value(empty) != m.mtp_head_pick_value(empty)  # NaN
     assert m.mtp_head_pick_key(float("-inf"), 2 ** 31 - 1) > empty
+
+
+def test_wait_limit_setter_returns_the_previous_limit(lib):
+    """The stage-wait limit is process-wide state: 2 s by default, and every set returns the
+    limit it replaces (nothing is launched here)."""
+    prev = m.mtp_head_set_wait_limit_ns(5)
+    try:
+        assert prev == 2_000_000_000
+        assert m.mtp_head_set_wait_limit_ns(0) == 5
+        assert m.mtp_head_set_wait_limit_ns(7) == 0
+    finally:
+        assert m.mtp_head_set_wait_limit_ns(prev) == 7
+    assert m.mtp_head_set_wait_limit_ns(prev) == prev
