@@ -8,6 +8,8 @@ columns of the full sweep's logits bit for bit, and the combined draft and its v
 the full sweep's draft and maximum. Rows planted on both sides of every shard boundary tie for
 the maximum, so a tie across a boundary must go to the lower index. The draft is also checked
 against the oracle's logits."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -152,3 +154,36 @@ def test_all_nan_sequence_gives_empty_keys_and_draft_minus_one():
     assert int(picks[0, 1]) == -2 ** 63 and int(picks[1, 1]) == -2 ** 63
     assert int(draft[1]) == -1
     assert 0 <= int(draft[0]) < V
+
+
+@pytest.mark.parametrize("R", [1, 7, 33, 1000])
+def test_pick_combine_many_keys(R):
+    """The combine kernel over R shards' keys for 16 sequences (a lane loop and a shuffle tree when
+    R > 32): keys made on the host from random (value, global index) pairs with ties, +-0, +-inf
+    and empty picks; the draft and value must be those of the largest key, which is the argmax
+    order's winner (larger value, then lower index; -1 and NaN when every key is empty)."""
+    B = 16
+    rng = np.random.default_rng(R)
+    vals = np.round(rng.standard_normal((R, B)) * 2).astype(np.float32)
+    vals[rng.random((R, B)) < 0.05] = np.float32(-0.0)
+    vals[rng.random((R, B)) < 0.02] = np.float32(np.inf)
+    vals[rng.random((R, B)) < 0.02] = np.float32(-np.inf)
+    idx = rng.integers(0, 2 ** 31 - 1, (R, B))
+    empty = rng.random((R, B)) < 0.1
+    empty[:, 3] = True  # sequence 3: every shard empty
+    keys = np.array([[m.mtp_head_pick_key(float(vals[r, b]), -1 if empty[r, b] else int(idx[r, b])) for b in range(B)]
+                     for r in range(R)], dtype=np.int64)
+    draft = torch.full((B,), -5, dtype=torch.int32, device=DEV)
+    value = torch.empty(B, dtype=torch.float32, device=DEV)
+    m.mtp_head_pick_combine(torch.from_numpy(keys).to(DEV), draft, value)
+    torch.cuda.synchronize()
+    for b in range(B):
+        ok = ~empty[:, b]
+        if not ok.any():
+            assert int(draft[b]) == -1 and math.isnan(float(value[b]))
+            continue
+        v, i = vals[ok, b].astype(np.float64), idx[ok, b]
+        best = v.max()
+        want = int(i[v == best].min())
+        assert int(draft[b]) == want
+        assert float(value[b]) == best
