@@ -403,8 +403,8 @@ def run_ours(args, world, rank, local):
         cwsb = m.context_workspace(b, H, dev)
         graph_buffers.append(cwsb)
 
-        # the input stage alone as the chain runs it: with room for a prebuilt concat (built once by
-        # the row-parallel kernel for B >= 6), which the context-row entry point gives it at R <= 16
+        # the input stage alone as the whole step runs it: the context-row path (concat kernel,
+        # tcgen05 GEMM, partial reduce), a new token row each call
         def input_b(n, tokb=tokb, hidden_b=hidden_b, xb=xb, cwsb=cwsb):
             def fn(st):
                 for i in range(n):
@@ -655,7 +655,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": 2 * K,  # the BF16 chain region `value` is timed on: 2 kernels per step
         "gpu_launches_all_timed_regions": launches_all,
         "clocks": clocks.summary(),
-        "batched": dict(batched, steps=Kb, kernels="tensor-core input stage and sweep (mma.sync)",
+        "batched": dict(batched, steps=Kb, kernels="input stage: context-row tcgen05 GEMM; sweep: mma.sync tensor-core kernel",
                         timing="Kb-step chains / sweep loops in one CUDA graph each; frac of the measured peak"),
         "context": dict(context, steps=Kb, peak_tflops=tc_peak, peak_source=tc_src,
                         kernels="row-parallel concat + tcgen05 GEMM x = concat . eh_proj^T (FP32 accumulator)",

@@ -64,7 +64,7 @@ def test_workspace_bytes(lib):
     assert m.mtp_head_workspace_bytes(0, 6144, 154880) == 0
     assert m.mtp_head_workspace_bytes(17, 6144, 154880) == 0
     assert m.mtp_head_workspace_bytes(1, 0, 10) == 0
-    # the whole-step workspace also has room for the batched input stage's prebuilt concat
+    # the whole-step workspace also has room for the context-row input stage (the concat of the B rows, at least)
     assert m.mtp_head_workspace_bytes(16, 6144, 154880) >= 128 + 8192 * 16 + 16 * 2 * 6144 * 2 + 16 * 4
 
 
