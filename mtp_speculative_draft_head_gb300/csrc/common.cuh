@@ -124,6 +124,11 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x, int 
                "r"(x), "r"(y)
                : "memory");
 }
+// Prefetch `bytes` contiguous bytes into L2 only (a hint: no completion to wait for). Address
+// and size must be multiples of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -305,32 +310,55 @@ __device__ __forceinline__ void arg_update(ArgBest& b, float v, int32_t i) {
 }
 
 // Last step of the grid argmax: combine the per-CTA partials part[g * nb + b] (g < ncta) into
-// draft[b]. One warp per sequence; its lanes read partials g = lane, lane + 32, ... at once
-// (a single thread walking all partials waited out one L2 latency per CTA, ~30 us for 152)
-// and a shuffle tree combines them. (value, lowest index) is a total order, so the result does
-// not depend on the order. All threads of the block call it.
+// draft[b]. A warp takes two sequences per pass; each lane loads its partials g = lane,
+// lane + 32, ... of both (up to kCombineLoads apiece) before it compares any, so a pass waits
+// out one L2 round trip, and a shuffle tree combines the lanes. (A single thread walking all
+// partials waited out one L2 latency per CTA, ~30 us for 152; a warp per sequence with one load
+// in flight per lane still cost ~1 us more per sweep than this.) (value, lowest index) is a
+// total order, so the result does not depend on the order. All threads of the block call it.
 // A vocabulary shard's sweep numbers its rows from index_base (the shard's first global row)
 // and may also store the pick's exchange key (pick.h) in pick[b]; draft and pick may be null.
 __device__ __forceinline__ void combine_partials(const ArgBest* part, unsigned int ncta, int nb, int32_t* draft,
                                                  int32_t index_base, int64_t* pick) {
+  constexpr int kCombineLoads = 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (int b = warp; b < nb; b += nw) {
-    ArgBest c{0.0f, -1};
-    for (unsigned int g = lane; g < ncta; g += 32) {
-      const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(part + static_cast<size_t>(g) * nb + b));
-      const int32_t i = static_cast<int32_t>(raw.y);
-      if (i >= 0) arg_update(c, __uint_as_float(raw.x), i);
+  for (int b0 = warp; b0 < nb; b0 += 2 * nw) {
+    ArgBest c[2] = {ArgBest{0.0f, -1}, ArgBest{0.0f, -1}};
+    for (unsigned int g0 = lane; g0 < ncta; g0 += 32 * kCombineLoads) {
+      uint2 raw[2][kCombineLoads];
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int j = 0; j < kCombineLoads; ++j) {
+          const unsigned int g = g0 + 32 * j;
+          const int b = b0 + s * nw;
+          raw[s][j] = (g < ncta && b < nb) ? __ldcg(reinterpret_cast<const uint2*>(part + static_cast<size_t>(g) * nb + b))
+                                           : make_uint2(0u, 0xffffffffu);  // index -1: no candidate
+        }
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int j = 0; j < kCombineLoads; ++j) {
+          const int32_t i = static_cast<int32_t>(raw[s][j].y);
+          if (i >= 0) arg_update(c[s], __uint_as_float(raw[s][j].x), i);
+        }
     }
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1) {
-      const float v = __shfl_xor_sync(0xffffffffu, c.v, m);
-      const int32_t i = __shfl_xor_sync(0xffffffffu, c.i, m);
-      if (i >= 0) arg_update(c, v, i);
-    }
-    if (lane == 0) {
-      const int32_t g = c.i >= 0 ? c.i + index_base : -1;
-      if (draft != nullptr) draft[b] = g;
-      if (pick != nullptr) pick[b] = pick_key(c.v, g);
+    for (int s = 0; s < 2; ++s) {
+      const int b = b0 + s * nw;  // the same for the whole warp
+      if (b >= nb) break;
+      ArgBest r = c[s];
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) {
+        const float v = __shfl_xor_sync(0xffffffffu, r.v, m);
+        const int32_t i = __shfl_xor_sync(0xffffffffu, r.i, m);
+        if (i >= 0) arg_update(r, v, i);
+      }
+      if (lane == 0) {
+        const int32_t g = r.i >= 0 ? r.i + index_base : -1;
+        if (draft != nullptr) draft[b] = g;
+        if (pick != nullptr) pick[b] = pick_key(r.v, g);
+      }
     }
   }
 }
