@@ -513,12 +513,14 @@ def run_ours(args, world, rank, local):
             barrier(world)
             results[key] = timed_graph(g, torch.cuda.current_stream())
             barrier(world)
-            launches_all += 2 * Kb if key[1] == "chain" else Kb  # (B >= 6 input stages: 2 kernels, not counted)
+            # kernels per call at B >= 2: the input stage is the context-row path (concat, tcgen05
+            # GEMM, partial reduce: 3), the sweep the norm parts and the tensor-core sweep (2)
+            launches_all += {"chain": 5, "sweep": 2, "input": 3}[key[1]] * Kb
         for r, g in cgraphs.items():
             barrier(world)
             results[("context", r)] = timed_graph(g, torch.cuda.current_stream())
             barrier(world)
-            launches_all += 2 * Kb
+            launches_all += 3 * Kb  # concat, GEMM, partial reduce (every R here splits along k)
         barrier(world)
         results["quantize"] = timed_graph(qgraph, torch.cuda.current_stream())
         barrier(world)

@@ -135,7 +135,8 @@ size_t mtp_head_context_workspace_bytes(int R, int H);
  * Output stage ("glm5next_mtp_head.rs", `forward_one`: `shared_head.norm` in place, then the
  * `lm_head` dense gemv -- or `dense_gemv_fp8w` over the FP8 copy described in the `head_fp8`
  * doc -- then `argmax_bf16`; here the sweep covers the whole vocabulary on one GPU and the
- * argmax is fused into it). One kernel per call; lm_head is read once for all B sequences.
+ * argmax is fused into it). One sweep kernel per call, which reads lm_head once for all B
+ * sequences; for B = 2..16 a small kernel before it sums the squares of x's rows (for the norm).
  *
  *   x              [B, H]  BF16   block output
  *   final_norm_w   [H]     BF16   shared_head.norm weight
@@ -146,10 +147,10 @@ size_t mtp_head_context_workspace_bytes(int R, int H);
  *                                 -1 if every logit of that sequence is NaN
  *   status         [1]     int32  optional (may be NULL); MTP_ERR_TIMEOUT on a kernel-side wait
  *   workspace             device scratch of at least mtp_head_workspace_bytes(B, H, V)
- *                         bytes, zero-filled once before its first use. The kernel returns it
- *                         to zero itself, so it stays valid across calls and CUDA-graph
- *                         replays. Two calls that may run at the same time (different streams)
- *                         need different workspaces.
+ *                         bytes, zero-filled once before its first use. The kernels return
+ *                         its counters to zero themselves, so it stays valid across calls and
+ *                         CUDA-graph replays. Two calls that may run at the same time
+ *                         (different streams) need different workspaces.
  * ---------------------------------------------------------------------------------------- */
 int mtp_head_logits_argmax_batched(const uint16_t* x, const uint16_t* final_norm_w,
                                    const void* lm_head, const float* row_scale, int w_dtype,
@@ -217,7 +218,7 @@ float mtp_head_pick_value(int64_t key);
  * its own, or a process whose device memory was all claimed up front by another allocator.
  * It computes exactly what mtp_head_logits_argmax_batched computes (same kernels, same
  * arguments minus workspace / workspace_bytes) and allocates nothing: the workspace is a fixed
- * device array inside the library, 131,200 bytes, enough for the largest batch (B <= 16);
+ * device array inside the library, 133,248 bytes, enough for the largest batch (B <= 16);
  * every GPU that loads the library holds it until the process exits. B outside 1..16 returns
  * MTP_ERR_SHAPE before anything runs.
  *   - The first call on a device looks up that array's device address (once per device, with

@@ -17,8 +17,8 @@
 
 namespace {
 
-// 128-byte header + one 8-byte partial per CTA (at most 1024) and sequence (at most 16):
-// the workspace of the largest call the output stage accepts.
+// The 2176-byte header + one 8-byte partial per CTA (at most 1024) and sequence (at most 16):
+// the workspace of the largest call the output stage accepts (133,248 bytes).
 constexpr size_t kStaticScratchBytes =
     static_cast<size_t>(mtp::kWsHeader) + static_cast<size_t>(mtp::kMaxGrid) * mtp::kMaxB * 8;
 

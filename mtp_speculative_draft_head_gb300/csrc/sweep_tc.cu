@@ -15,7 +15,8 @@
 //    full/empty pairs, bounded waits);
 //  * 3 builder warps: compute xhat = rms_norm_vanilla(x, final_norm_w) one stage at a time
 //    (BF16 for a BF16 head; for FP8, f16 scaled by 2^k per sequence, exact) into a small ring, in
-//    the same swizzled layout, with the same exact rounding as the other kernels;
+//    the same swizzled layout, with the same exact rounding as the other kernels. The sums of
+//    squares behind 1/rms come from a small kernel launched just before (xnorm_parts_kernel);
 //  * 8 consumer warps: 16 rows each of a 128-row tile; ldmatrix + mma.sync, batch as N (8 or 16).
 // Loop order: groups of 4 row tiles; per stage the activations are built once and used by every
 // tile of the group, whose accumulators stay in registers. Each lm_head byte is read once.
@@ -58,7 +59,6 @@ constexpr int kAStageBytes = kKS * kATileBytes;    // 32 KB
 constexpr int kAStages = 6;
 constexpr int kSeq = 16;                           // activation rows per B tile (N <= 16)
 constexpr int kProducerWarp = kConsumerWarps + kBuilderWarps;
-constexpr int kBarXRead = 3;  // named barrier: prologue has read x (prologue -> producer)
 
 template <int WT>
 struct TcCfg {
@@ -142,8 +142,9 @@ struct BFrags<MTP_W_FP8_E4M3, NT> {
   }
 };
 
-// CTA combine of per-warp bests (wbest[warp * kSeq + b]) and the last-CTA-done grid argmax.
-__device__ void tc_argmax_finish(int nb, const ArgBest* wbest, const SweepArgs& a) {
+// CTA combine of per-warp bests (wbest[warp * kSeq + b]) and the last-CTA-done grid argmax
+// (scratch: kTcThreads entries of shared memory no longer in use).
+__device__ void tc_argmax_finish(int nb, const ArgBest* wbest, const SweepArgs& a, ArgBest* scratch) {
   uint8_t* ws = a.ws;
   __shared__ int is_last;
   ArgBest* part = reinterpret_cast<ArgBest*>(ws + kWsHeader);
@@ -162,9 +163,66 @@ __device__ void tc_argmax_finish(int nb, const ArgBest* wbest, const SweepArgs& 
   __syncthreads();
   if (is_last) {
     __threadfence();
-    combine_partials(part, gridDim.x, nb, a.draft, a.index_base, a.pick);
+    combine_partials_coalesced(part, gridDim.x, nb, a.draft, a.index_base, a.pick, scratch);
     if (threadIdx.x == 0) atomicExch(counter, 0u);
   }
+}
+
+// ---------------------------------------------------------------------------- norm parts
+// The sums of squares behind shared_head.norm's 1/rms (and, for an FP8 head, max |x w_f|, which
+// fixes the power-of-two scale of the f16 activations) of every row of x, computed once per call
+// instead of in each of the sweep's CTAs: there, every CTA summed all B rows itself, 152 times
+// the same double-float work, ~9 us of the sweep at B = 16. One warp per slice of a row
+// (grid kNormParts x B); each writes {sum hi, sum lo, max, 0} to the workspace header, and the
+// sweep adds a row's kNormParts slices in order. At most 32 registers a thread and no shared
+// memory, so a CTA of it fits on an SM beside a running sweep CTA (which leaves ~1000 registers
+// free): it starts while the kernel before is still finishing and never keeps a sweep CTA off
+// its SM. Measured at H = 6144 (one GB300, 50-launch CUDA graphs), the same drafts: the FP8
+// sweep at B = 16 from 165.5 to 160.3 us, BF16 from 298.5 to 290.6 us, and the whole batched
+// step 205 -> 199.7 us (FP8) and 333 -> 325.7 us (BF16). A version with 256-thread CTAs was
+// slower for the sweep alone (FP8 B = 16: 165 -> 168.6 us): its CTAs kept 16 SMs from the sweep
+// for their run, and those SMs' CTAs finished last.
+template <int WT>
+__global__ void __maxnreg__(32) xnorm_parts_kernel(const SweepArgs a) {
+  const int p = blockIdx.x, b = blockIdx.y, lane = threadIdx.x, H = a.H;
+  // the sweep may launch at once: its CTAs wait for this grid before they read the parts
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();  // x comes from the preceding kernel
+  const int nv = H >> 3;  // 16-byte vectors of a row
+  const int v0 = static_cast<int>(static_cast<int64_t>(nv) * p / kNormParts);
+  const int v1 = static_cast<int>(static_cast<int64_t>(nv) * (p + 1) / kNormParts);
+  const uint4* xv = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(b) * H);
+  const uint4* wv = reinterpret_cast<const uint4*>(a.final_norm_w);
+  DF acc{0.0f, 0.0f};
+  float mx = 0.0f;
+#pragma unroll 3
+  for (int v = v0 + lane; v < v1; v += 32) {
+    const uint4 q = xv[v];
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float lo = bf16_lo(u[t]), hi = bf16_hi(u[t]);
+      df_add(acc, __fmul_rn(lo, lo));  // squares of BF16 values are exact in fp32
+      df_add(acc, __fmul_rn(hi, hi));
+    }
+    if constexpr (WT == MTP_W_FP8_E4M3) {
+      const uint4 wq = wv[v];
+      const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        mx = fmaxf(mx, fabsf(__fmul_rn(bf16_lo(u[t]), bf16_lo(w4[t]))));
+        mx = fmaxf(mx, fabsf(__fmul_rn(bf16_hi(u[t]), bf16_hi(w4[t]))));
+      }
+    }
+  }
+  // fixed butterfly: the result does not depend on timing
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) {
+    acc = df_add(acc, shfl_xor_df(acc, m));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+  }
+  if (lane == 0)
+    reinterpret_cast<float4*>(a.ws + kWsNormOffset)[b * kNormParts + p] = make_float4(acc.hi, acc.lo, mx, 0.0f);
 }
 
 // ---------------------------------------------------------------------------- the kernel
@@ -217,10 +275,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer
-    // The weight stream starts once the prologue has read x: issued first, ~30 MB of tensor
-    // loads over all SMs sit in front of those few loads in the memory queues and the prologue
-    // (hence the first MMA) comes several microseconds later.
-    asm volatile("bar.sync %0, %1;" ::"r"(kBarXRead), "r"(kPrologueThreads + 32) : "memory");
+    // lm_head does not depend on the kernels before: the weight stream starts at once, while
+    // the prologue waits for the norm parts. (When the prologue itself summed the squares of
+    // all of x, the stream had to wait for those reads: ~30 MB of tensor loads in front of them
+    // in the memory queues delayed them by several microseconds.)
     int issued = 0;
     if (lane == 0) {
       const uint64_t policy = l2_evict_first_policy();
@@ -259,20 +317,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ prologue (warps 0..11)
-    pdl_wait_prior_grid();  // x comes from the preceding kernel
+    pdl_wait_prior_grid();  // the norm parts (and x) come from the preceding kernels
     {
-      // the activation ring is free until the builders start: scratch of the sums of squares
-      DF* part = reinterpret_cast<DF*>(bring);
-      float* mpart = reinterpret_cast<float*>(part + kPrologueThreads);
-      DF* tot = reinterpret_cast<DF*>(mpart + kPrologueThreads);
-      float* mtot = reinterpret_cast<float*>(tot + kSeq);
-      auto row = [&](int b) -> const uint16_t* { return a.x + static_cast<size_t>(b) * H; };
-      sumsq_rows<kPrologueThreads, 8, WT == MTP_W_FP8_E4M3>(B, H, row, a.final_norm_w, part, mpart, tot, mtot, 1);
-      asm volatile("bar.arrive %0, %1;" ::"r"(kBarXRead), "r"(kPrologueThreads + 32) : "memory");
       if (threadIdx.x < B) {
         const int b = threadIdx.x;
+        // a row's slices in order: the sum does not depend on timing
+        const float4* pp = reinterpret_cast<const float4*>(a.ws + kWsNormOffset) + b * kNormParts;
+        DF tot{0.0f, 0.0f};
+        float mtot = 0.0f;
+        for (int q = 0; q < kNormParts; ++q) {
+          const float4 v = __ldcg(pp + q);
+          tot = df_add(tot, DF{v.x, v.y});
+          mtot = fmaxf(mtot, v.z);
+        }
         // 1 / rms in fp64 (rsqrt: within an ulp or two of the correctly rounded value)
-        const double ms = (static_cast<double>(tot[b].hi) + static_cast<double>(tot[b].lo)) * a.inv_h;
+        const double ms = (static_cast<double>(tot.hi) + static_cast<double>(tot.lo)) * a.inv_h;
         const double rr = rsqrt(ms + static_cast<double>(a.eps));
         const float rh = static_cast<float>(rr);
         const float rl = static_cast<float>(rr - static_cast<double>(rh));
@@ -281,7 +340,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float xs = 1.0f, us = 1.0f;
         if constexpr (WT == MTP_W_FP8_E4M3) {
           // largest |xhat| of this sequence: rounding is monotonic, so it is the rounded max
-          const float mx = mtot[b];
+          const float mx = mtot;
           const float yh = __fmul_rn(mx, rh);
           const float yl = __fmaf_rn(mx, rl, __fmaf_rn(mx, rh, -yh));
           const float m = bf16_bits_to_f32(bf16_rne_df(yh, yl));
@@ -476,7 +535,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   __syncthreads();
   pdl_wait_prior_grid();  // the workspace may still be read by the kernel before (no-op if done)
-  tc_argmax_finish(B, wbest, a);
+  tc_argmax_finish(B, wbest, a, reinterpret_cast<ArgBest*>(aring));  // the weight ring is idle now
 }
 
 // ---------------------------------------------------------------------------- host side
@@ -526,6 +585,14 @@ cudaError_t launch_sweep_tc(const SweepArgs& a, cudaStream_t stream, bool* launc
   if (g > kMaxGrid) g = kMaxGrid;
   const unsigned grid = static_cast<unsigned>(g < 1 ? 1 : g);
   *launched = true;
+  {
+    SweepArgs na = a;
+    void* nparams[] = {&na};
+    const void* nk = a.w_dtype == MTP_W_BF16 ? reinterpret_cast<const void*>(xnorm_parts_kernel<MTP_W_BF16>)
+                                             : reinterpret_cast<const void*>(xnorm_parts_kernel<MTP_W_FP8_E4M3>);
+    err = launch_pdl(nk, dim3(kNormParts, a.B), dim3(32), 0, stream, nparams);
+    if (err != cudaSuccess) return err;
+  }
   if (a.w_dtype == MTP_W_BF16)
     return a.B <= 8 ? launch_tc<MTP_W_BF16, 1>(a, tm, grid, smem, stream) : launch_tc<MTP_W_BF16, 2>(a, tm, grid, smem, stream);
   return a.B <= 8 ? launch_tc<MTP_W_FP8_E4M3, 1>(a, tm, grid, smem, stream)
