@@ -297,6 +297,43 @@ int mtp_head_forward_host(const uint16_t* embed, const uint16_t* enorm_w,
                           float eps, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * The same step with the arguments that stay fixed from call to call gathered in one struct
+ * (no counterpart on the source pages, like mtp_head_forward_host itself, whose shape is
+ * `forward_one`'s). For a caller that makes the same draft step over and over through a costly
+ * call boundary -- a language binding marshals 23 arguments per call, ~3 us from Python --
+ * a step then passes four. The fields mean what the parameters of mtp_head_forward_host of the
+ * same names mean; mtp_head_forward_host_args(a, tokens_host, hidden_host, draft_host) is
+ * exactly mtp_head_forward_host(a->embed, ..., tokens_host, hidden_host, a->tokens_dev, ...,
+ * draft_host, a->status, ..., a->stream): the same work, results and status codes, plus
+ * MTP_ERR_ARG for a NULL `a`. The struct is read during the call only.
+ * ---------------------------------------------------------------------------------------- */
+typedef struct mtp_host_step_args {
+  const uint16_t* embed;
+  const uint16_t* enorm_w;
+  const uint16_t* hnorm_w;
+  const uint16_t* eh_proj;
+  const uint16_t* final_norm_w;
+  const void* lm_head;
+  const float* row_scale;
+  int w_dtype;
+  int32_t* tokens_dev;
+  uint16_t* hidden_dev;
+  uint16_t* x_dev;
+  int32_t* draft_dev;
+  int32_t* status;
+  void* workspace;
+  size_t workspace_bytes;
+  int B;
+  int H;
+  int V;
+  float eps;
+  void* stream;
+} mtp_host_step_args;
+
+int mtp_head_forward_host_args(const mtp_host_step_args* a, const int32_t* tokens_host,
+                               const uint16_t* hidden_host, int32_t* draft_host);
+
+/* ------------------------------------------------------------------------------------------
  * FP8 E4M3 copy of a [V, H] BF16 matrix ("glm5next_mtp_head.rs", `head_fp8` doc: an E4M3
  * copy of lm_head used for drafting only). Per row v:
  *   row_scale[v] = fp32( max_k |w[v, k]| / 448 )

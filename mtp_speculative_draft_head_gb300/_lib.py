@@ -41,6 +41,7 @@ SIGNATURES = {
     "mtp_head_workspace_bytes": (Z, [I, I, I]),
     "mtp_head_forward_batched": (I, [P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, Z, I, I, I, F, P]),
     "mtp_head_forward_host": (I, [P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, P, P, Z, I, I, I, F, P]),
+    "mtp_head_forward_host_args": (I, [P, P, P, P]),
     "mtp_head_quantize_fp8": (I, [P, P, P, P, I, I, P]),
     "mtp_head_context_rows": (I, [P, P, P, P, P, P, P, P, P, Z, I, I, I, F, P]),
     "mtp_head_context_workspace_bytes": (Z, [I, I]),
@@ -287,10 +288,19 @@ def mtp_head_forward_host(embed, enorm_w, hnorm_w, eh_proj, final_norm_w, lm_hea
         "mtp_head_forward_host")
 
 
+class _HostStepArgs(ctypes.Structure):
+    """mtp_host_step_args (include/mtp_head.h), field for field."""
+    _fields_ = [("embed", P), ("enorm_w", P), ("hnorm_w", P), ("eh_proj", P), ("final_norm_w", P),
+                ("lm_head", P), ("row_scale", P), ("w_dtype", I), ("tokens_dev", P), ("hidden_dev", P),
+                ("x_dev", P), ("draft_dev", P), ("status", P), ("workspace", P), ("workspace_bytes", Z),
+                ("B", I), ("H", I), ("V", I), ("eps", F), ("stream", P)]
+
+
 class HostStep:
     """mtp_head_forward_host with its device buffers bound once: a call passes only the three host
-    buffers (tensors, or their addresses as ints), so a synchronous draft step costs one ctypes
-    call on the host. The bound tensors stay referenced for the object's lifetime."""
+    buffers (tensors, or their addresses as ints) to mtp_head_forward_host_args, so a synchronous
+    draft step costs one four-argument ctypes call on the host. The bound tensors stay referenced
+    for the object's lifetime."""
 
     def __init__(self, embed, enorm_w, hnorm_w, eh_proj, final_norm_w, lm_head, row_scale, w_dtype: int,
                  tokens_dev, hidden_dev, x_dev, draft_dev, ws, status=None, eps: float = 1e-6, stream=None):
@@ -299,20 +309,20 @@ class HostStep:
         self.B, self.H, self.V = B, H, V
         self._keep = (embed, enorm_w, hnorm_w, eh_proj, final_norm_w, lm_head, row_scale, tokens_dev,
                       hidden_dev, x_dev, draft_dev, ws, status, stream)
-        self._fn = load().mtp_head_forward_host
-        self._head = (_dev(embed, "embed"), _dev(enorm_w, "enorm_w"), _dev(hnorm_w, "hnorm_w"),
-                      _dev(eh_proj, "eh_proj"), _dev(final_norm_w, "final_norm_w"), _dev(lm_head, "lm_head"),
-                      _dev(row_scale, "row_scale"), int(w_dtype))
-        self._mid = (_dev(tokens_dev, "tokens_dev"), _dev(hidden_dev, "hidden_dev"), _dev(x_dev, "x_dev"),
-                     _dev(draft_dev, "draft_dev"))
-        self._tail = (_dev(status, "status"), _dev(ws, "workspace"), ws.numel() * ws.element_size(), B, H, V,
-                      float(eps), _stream(stream))
+        self._fn = load().mtp_head_forward_host_args
+        self._args = _HostStepArgs(
+            _dev(embed, "embed"), _dev(enorm_w, "enorm_w"), _dev(hnorm_w, "hnorm_w"), _dev(eh_proj, "eh_proj"),
+            _dev(final_norm_w, "final_norm_w"), _dev(lm_head, "lm_head"), _dev(row_scale, "row_scale"),
+            int(w_dtype), _dev(tokens_dev, "tokens_dev"), _dev(hidden_dev, "hidden_dev"), _dev(x_dev, "x_dev"),
+            _dev(draft_dev, "draft_dev"), _dev(status, "status"), _dev(ws, "workspace"),
+            ws.numel() * ws.element_size(), B, H, V, float(eps), _stream(stream))
+        self._addr = ctypes.addressof(self._args)
 
     def __call__(self, tokens_host, hidden_host, draft_host) -> None:
         t = tokens_host if isinstance(tokens_host, int) else tokens_host.data_ptr()
         h = hidden_host if isinstance(hidden_host, int) else hidden_host.data_ptr()
         d = draft_host if isinstance(draft_host, int) else draft_host.data_ptr()
-        code = self._fn(*self._head, t, h, *self._mid, d, *self._tail)
+        code = self._fn(self._addr, t, h, d)
         if code != OK:
             raise MTPError(code, "mtp_head_forward_host")
 

@@ -517,6 +517,15 @@ int mtp_head_forward_host(const uint16_t* embed, const uint16_t* enorm_w, const 
   return run_host_step(hs, tokens_host, hidden_host, draft_host);
 }
 
+int mtp_head_forward_host_args(const mtp_host_step_args* a, const int32_t* tokens_host, const uint16_t* hidden_host,
+                               int32_t* draft_host) {
+  if (a == nullptr) return MTP_ERR_ARG;
+  return mtp_head_forward_host(a->embed, a->enorm_w, a->hnorm_w, a->eh_proj, a->final_norm_w, a->lm_head, a->row_scale,
+                               a->w_dtype, tokens_host, hidden_host, a->tokens_dev, a->hidden_dev, a->x_dev,
+                               a->draft_dev, draft_host, a->status, a->workspace, a->workspace_bytes, a->B, a->H,
+                               a->V, a->eps, a->stream);
+}
+
 size_t mtp_head_context_workspace_bytes(int R, int H) {
   if (R < 1 || R > kMaxContextRows || H < 1 || H > 65536) return 0;
   return mtp::context_workspace_bytes(R, H);

@@ -33,6 +33,7 @@ def test_header_declares_the_entry_points():
     for name in ("mtp_head_input", "mtp_head_input_batched", "mtp_head_logits_argmax",
                  "mtp_head_logits_argmax_batched", "mtp_head_quantize_fp8",
                  "mtp_head_workspace_bytes", "mtp_head_forward_batched", "mtp_head_forward_host",
+                 "mtp_head_forward_host_args",
                  "mtp_head_context_rows", "mtp_head_context_workspace_bytes",
                  "mtp_head_logits_argmax_batched_noalloc", "mtp_head_logits_argmax_shard",
                  "mtp_head_pick_combine", "mtp_head_pick_key", "mtp_head_pick_index", "mtp_head_pick_value",
@@ -160,6 +161,38 @@ def test_forward_host_validation(lib):
     bad = list(args)
     bad[18] = 0  # B
     assert f(*bad) == m.ERR_SHAPE
+
+
+# mtp_host_step_args field -> position of the same argument of mtp_head_forward_host
+_HOST_FIELDS = {"embed": 0, "enorm_w": 1, "hnorm_w": 2, "eh_proj": 3, "final_norm_w": 4, "lm_head": 5,
+                "row_scale": 6, "w_dtype": 7, "tokens_dev": 10, "hidden_dev": 11, "x_dev": 12, "draft_dev": 13,
+                "status": 15, "workspace": 16, "workspace_bytes": 17, "B": 18, "H": 19, "V": 20, "eps": 21,
+                "stream": 22}
+
+
+@pytest.mark.parametrize("field,value", [
+    ("embed", None), ("enorm_w", None), ("hnorm_w", None), ("eh_proj", A + 2), ("final_norm_w", None),
+    ("lm_head", A + 8), ("row_scale", A + 2), ("w_dtype", 7), ("tokens_dev", None), ("hidden_dev", A + 4),
+    ("x_dev", None), ("draft_dev", A + 2), ("status", A + 1), ("workspace", None), ("workspace_bytes", 16),
+    ("B", 0), ("B", 17), ("H", 0), ("V", 0), ("eps", float("nan")), ("eps", -1.0),
+])
+def test_forward_host_args_reads_every_field(lib, field, value):
+    # each variant breaks one field; both entry points must reject it with the same status before
+    # anything runs, which they can only do if the struct's layout matches the header
+    base = [A, A, A, A, A, A, None, m.W_BF16, A, A, A, A, A, A, A, None, A, 1 << 20, 1, 64, 100, 1e-6, None]
+    fh = list(base)
+    fh[_HOST_FIELDS[field]] = value
+    want = lib.mtp_head_forward_host(*[ctypes.c_float(v) if i == 21 else v for i, v in enumerate(fh)])
+    assert want in (m.ERR_ARG, m.ERR_SHAPE, m.ERR_ALIGN, m.ERR_WORKSPACE)  # rejected before any CUDA call
+    sa = m._lib._HostStepArgs(*[fh[i] for i in _HOST_FIELDS.values()])
+    assert lib.mtp_head_forward_host_args(ctypes.addressof(sa), fh[8], fh[9], fh[14]) == want
+
+
+def test_forward_host_args_null(lib):
+    assert lib.mtp_head_forward_host_args(None, A, A, A) == m.ERR_ARG
+    sa = m._lib._HostStepArgs(A, A, A, A, A, A, None, m.W_BF16, A, A, A, A, None, A, 1 << 20, 0, 64, 100, 1e-6,
+                              None)
+    assert lib.mtp_head_forward_host_args(ctypes.addressof(sa), None, A, A) == m.ERR_ARG  # tokens_host
 
 
 def _context(lib, **kw):
