@@ -218,7 +218,7 @@ float mtp_head_pick_value(int64_t key);
  * its own, or a process whose device memory was all claimed up front by another allocator.
  * It computes exactly what mtp_head_logits_argmax_batched computes (same kernels, same
  * arguments minus workspace / workspace_bytes) and allocates nothing: the workspace is a fixed
- * device array inside the library, 133,248 bytes, enough for the largest batch (B <= 16);
+ * device array inside the library, 2,304 bytes, enough for any batch (B <= 16);
  * every GPU that loads the library holds it until the process exits. B outside 1..16 returns
  * MTP_ERR_SHAPE before anything runs.
  *   - The first call on a device looks up that array's device address (once per device, with
@@ -240,7 +240,7 @@ int mtp_head_logits_argmax_batched_noalloc(const uint16_t* x, const uint16_t* fi
                                            void* stream);
 
 /* Bytes of workspace for the output stage and the whole-step entry points (no device query; 0
- * for invalid shapes): the output stage's part (the first 128 + 8192 * B bytes, which must be
+ * for invalid shapes): the output stage's part (the first 2304 bytes for any B, which must be
  * zero-filled once), then, 256-byte aligned, room for the context-row path's workspace of B rows
  * (mtp_head_context_workspace_bytes(B, H): concat, row flags and FP32 partial sums; no
  * initialisation needed). The output stage alone accepts any workspace of at least its own part.

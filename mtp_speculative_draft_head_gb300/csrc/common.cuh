@@ -18,15 +18,16 @@
 namespace mtp {
 
 constexpr int kMaxB = 16;        // sequences per sweep
-constexpr int kMaxGrid = 1024;   // CTAs per launch (bounds the workspace)
-// Output-stage workspace: a header, then one 8-byte argmax partial per CTA and sequence.
-// Header: the grid's finished-CTA counter at byte 0, the next dynamically claimed row (B = 1) at
-// byte 64, and from byte 128 the batched sweep's norm parts: float4 {sum of squares hi, lo,
-// max |x w|, 0} for kNormParts slices of each of up to kMaxB rows of x.
+constexpr int kMaxGrid = 1024;   // CTAs per launch
+// Output-stage workspace (kWsBytes, whatever B): the grid's finished-CTA counter at byte 0, the
+// next dynamically claimed row (B = 1) at byte 64, from byte 128 each sequence's running pick
+// (uint64 [kMaxB], below), and from byte 256 the batched sweep's norm parts: float4 {sum of
+// squares hi, lo, max |x w|, 0} for kNormParts slices of each of up to kMaxB rows of x.
 constexpr int kRowCounterOffset = 64;
+constexpr int kWsPickOffset = 128;
 constexpr int kNormParts = 8;
-constexpr int kWsNormOffset = 128;
-constexpr int kWsHeader = kWsNormOffset + kMaxB * kNormParts * 16;  // 2176
+constexpr int kWsNormOffset = 256;
+constexpr int kWsBytes = kWsNormOffset + kMaxB * kNormParts * 16;  // 2304
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // give up a wait after 2 s
 
 // ------------------------------------------------------------------------------------------
@@ -315,110 +316,29 @@ __device__ __forceinline__ void arg_update(ArgBest& b, float v, int32_t i) {
   }
 }
 
-// Last step of the grid argmax: combine the per-CTA partials part[g * nb + b] (g < ncta) into
-// draft[b]. A warp takes two sequences per pass; each lane loads its partials g = lane,
-// lane + 32, ... of both (up to kCombineLoads apiece) before it compares any, so a pass waits
-// out one L2 round trip, and a shuffle tree combines the lanes. (A single thread walking all
-// partials waited out one L2 latency per CTA, ~30 us for 152; a warp per sequence with one load
-// in flight per lane still cost ~1 us more per sweep than this.) (value, lowest index) is a
-// total order, so the result does not depend on the order. All threads of the block call it.
-// A vocabulary shard's sweep numbers its rows from index_base (the shard's first global row)
-// and may also store the pick's exchange key (pick.h) in pick[b]; draft and pick may be null.
-__device__ __forceinline__ void combine_partials(const ArgBest* part, unsigned int ncta, int nb, int32_t* draft,
-                                                 int32_t index_base, int64_t* pick) {
-  constexpr int kCombineLoads = 8;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (int b0 = warp; b0 < nb; b0 += 2 * nw) {
-    ArgBest c[2] = {ArgBest{0.0f, -1}, ArgBest{0.0f, -1}};
-    for (unsigned int g0 = lane; g0 < ncta; g0 += 32 * kCombineLoads) {
-      uint2 raw[2][kCombineLoads];
-#pragma unroll
-      for (int s = 0; s < 2; ++s)
-#pragma unroll
-        for (int j = 0; j < kCombineLoads; ++j) {
-          const unsigned int g = g0 + 32 * j;
-          const int b = b0 + s * nw;
-          raw[s][j] = (g < ncta && b < nb) ? __ldcg(reinterpret_cast<const uint2*>(part + static_cast<size_t>(g) * nb + b))
-                                           : make_uint2(0u, 0xffffffffu);  // index -1: no candidate
-        }
-#pragma unroll
-      for (int s = 0; s < 2; ++s)
-#pragma unroll
-        for (int j = 0; j < kCombineLoads; ++j) {
-          const int32_t i = static_cast<int32_t>(raw[s][j].y);
-          if (i >= 0) arg_update(c[s], __uint_as_float(raw[s][j].x), i);
-        }
-    }
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      const int b = b0 + s * nw;  // the same for the whole warp
-      if (b >= nb) break;
-      ArgBest r = c[s];
-#pragma unroll
-      for (int m = 16; m > 0; m >>= 1) {
-        const float v = __shfl_xor_sync(0xffffffffu, r.v, m);
-        const int32_t i = __shfl_xor_sync(0xffffffffu, r.i, m);
-        if (i >= 0) arg_update(r, v, i);
-      }
-      if (lane == 0) {
-        const int32_t g = r.i >= 0 ? r.i + index_base : -1;
-        if (draft != nullptr) draft[b] = g;
-        if (pick != nullptr) pick[b] = pick_key(r.v, g);
-      }
-    }
-  }
+// The grid argmax across CTAs. Each CTA folds its best (value, row) of sequence b into a
+// running maximum in the workspace by one 64-bit atomic max of the pick's exchange key (pick.h:
+// its order is the argmax order, larger value first, then lower index; -0 counts as +0, and NaN
+// never gets a key), stored with the top bit flipped so that 0 -- a zero-filled workspace -- is
+// "no candidate yet". The last CTA to finish reads the B keys back (one load each), writes the
+// drafts (and, for a vocabulary shard, the keys themselves), and puts the words back to 0 for
+// the next launch. The maximum does not depend on the order of the atomics. (Before: each CTA
+// wrote its partial, and the last CTA loaded and combined all of them, ncta x B partials: ~2.7
+// to 4 us at B = 16 over 152 CTAs. The atomics took 0.6 to 3 us off every sweep, B = 1 to 16.)
+__device__ __forceinline__ void pick_publish(uint8_t* ws, int b, float v, int32_t row, int32_t index_base) {
+  if (row < 0) return;
+  const uint64_t k = static_cast<uint64_t>(pick_key(v, row + index_base)) ^ 0x8000000000000000ull;
+  atomicMax(reinterpret_cast<unsigned long long*>(ws + kWsPickOffset) + b, static_cast<unsigned long long>(k));
 }
 
-// The same for kernels with many sequences per launch: every thread of the block loads partials
-// (consecutive threads read consecutive partials, so a warp's loads take a few cache lines
-// rather than one line per lane), keeping the best per sequence -- thread t only ever sees
-// sequence t % nb -- then one warp per sequence combines its column of `scratch` (blockDim.x
-// entries of shared memory). At 16 sequences over 152 CTAs this took the last CTA's combine from
-// ~4 us to ~2.7 us. All threads of the block call it.
-__device__ __forceinline__ void combine_partials_coalesced(const ArgBest* part, unsigned int ncta, int nb,
-                                                           int32_t* draft, int32_t index_base, int64_t* pick,
-                                                           ArgBest* scratch) {
-  constexpr int kLoads = 8;
-  const int t = threadIdx.x;
-  const int nt = (static_cast<int>(blockDim.x) / nb) * nb;  // threads that load
-  ArgBest c{0.0f, -1};
-  if (t < nt) {
-    const int n = static_cast<int>(ncta) * nb;
-    for (int e0 = t; e0 < n; e0 += nt * kLoads) {
-      uint2 raw[kLoads];
-#pragma unroll
-      for (int j = 0; j < kLoads; ++j) {
-        const int e = e0 + j * nt;
-        raw[j] = e < n ? __ldcg(reinterpret_cast<const uint2*>(part + e)) : make_uint2(0u, 0xffffffffu);
-      }
-#pragma unroll
-      for (int j = 0; j < kLoads; ++j) {
-        const int32_t i = static_cast<int32_t>(raw[j].y);
-        if (i >= 0) arg_update(c, __uint_as_float(raw[j].x), i);
-      }
-    }
-  }
-  scratch[t] = c;
-  __syncthreads();
-  const int warp = t >> 5, lane = t & 31, nw = blockDim.x >> 5, per = nt / nb;
-  for (int b = warp; b < nb; b += nw) {
-    ArgBest r{0.0f, -1};
-    for (int k = lane; k < per; k += 32) {
-      const ArgBest o = scratch[b + k * nb];
-      if (o.i >= 0) arg_update(r, o.v, o.i);
-    }
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) {
-      const float v = __shfl_xor_sync(0xffffffffu, r.v, m);
-      const int32_t i = __shfl_xor_sync(0xffffffffu, r.i, m);
-      if (i >= 0) arg_update(r, v, i);
-    }
-    if (lane == 0) {
-      const int32_t g = r.i >= 0 ? r.i + index_base : -1;
-      if (draft != nullptr) draft[b] = g;
-      if (pick != nullptr) pick[b] = pick_key(r.v, g);
-    }
-  }
+// Last CTA: the pick of sequence b into draft[b] (a global index, -1 if no row had a number)
+// and pick[b] (may be null), and the running word back to 0.
+__device__ __forceinline__ void pick_finish(uint8_t* ws, int b, int32_t* draft, int64_t* pick) {
+  unsigned long long* kp = reinterpret_cast<unsigned long long*>(ws + kWsPickOffset) + b;
+  const int64_t key = static_cast<int64_t>(static_cast<uint64_t>(__ldcg(kp)) ^ 0x8000000000000000ull);
+  if (draft != nullptr) draft[b] = pick_index(key);
+  if (pick != nullptr) pick[b] = key;
+  *kp = 0ull;
 }
 
 // ------------------------------------------------------------------------------------------

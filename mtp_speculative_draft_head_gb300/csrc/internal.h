@@ -156,9 +156,9 @@ int check_output_args(const uint16_t* x, const uint16_t* final_norm_w, const voi
                       const int32_t* status, const void* workspace, size_t workspace_bytes, int B,
                       int H, int V, float eps);
 
-// Workspace layout of the output stage: a 2176-byte header (the CTA completion counter, the
-// row counter of the single-sequence sweep, the batched sweep's norm parts), then one
-// (value, index) partial per CTA and sequence.
+// Bytes of the output stage's workspace, the same for every B (2304: the CTA completion counter,
+// the row counter of the single-sequence sweep, each sequence's running pick, the batched
+// sweep's norm parts).
 size_t sweep_workspace_bytes(int B);
 
 }  // namespace mtp

@@ -1,11 +1,12 @@
 // Output stage for callers that cannot allocate device memory.
 //
-// mtp_head_logits_argmax_batched needs a small device workspace (a completion counter and one
-// (value, index) partial per CTA and sequence). Some callers cannot provide one: a plug-in that
+// mtp_head_logits_argmax_batched needs a small device workspace (a completion counter, each
+// sequence's running pick and the norm parts of the batched sweep). Some callers cannot provide
+// one: a plug-in that
 // only ever receives the buffers its host framework hands it and has no allocator of its own,
 // or a process whose device memory has all been claimed up front by another allocator. For them
-// this file keeps that workspace in a fixed device array owned by the library, sized for the
-// largest batch the output stage accepts, and runs the unchanged output-stage kernels on it.
+// this file keeps that workspace in a fixed device array owned by the library (the same size
+// for every batch the output stage accepts) and runs the unchanged output-stage kernels on it.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,10 +18,8 @@
 
 namespace {
 
-// The 2176-byte header + one 8-byte partial per CTA (at most 1024) and sequence (at most 16):
-// the workspace of the largest call the output stage accepts (133,248 bytes).
-constexpr size_t kStaticScratchBytes =
-    static_cast<size_t>(mtp::kWsHeader) + static_cast<size_t>(mtp::kMaxGrid) * mtp::kMaxB * 8;
+// The output stage's workspace (2304 bytes, the same for every batch size).
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(mtp::kWsBytes);
 
 // Every GPU that loads the library holds this array until the process exits. It is zero at load
 // time; each output-stage kernel returns its counter to zero, and each call clears it again
@@ -56,7 +55,7 @@ extern "C" int mtp_head_logits_argmax_batched_noalloc(const uint16_t* x, const u
                                                       int w_dtype, float* logits, int32_t* draft,
                                                       int32_t* status, int B, int H, int V, float eps,
                                                       void* stream) {
-  // the scratch holds the workspace of at most kMaxB sequences; larger requests are refused
+  // the scratch holds the workspace of any batch the output stage takes; others are refused
   if (B < 1 || B > mtp::kMaxB) return MTP_ERR_SHAPE;
   if (mtp::sweep_workspace_bytes(B) > kStaticScratchBytes) return MTP_ERR_WORKSPACE;
   void* ws = nullptr;
@@ -64,8 +63,8 @@ extern "C" int mtp_head_logits_argmax_batched_noalloc(const uint16_t* x, const u
   const int v = mtp::check_output_args(x, final_norm_w, lm_head, row_scale, w_dtype, logits, draft,
                                        status, ws, kStaticScratchBytes, B, H, V, eps);
   if (v != MTP_OK) return v;
-  // the completion counter must start at zero (the partials are always written before use)
-  if (cudaMemsetAsync(ws, 0, mtp::kWsHeader, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  // the completion counter and the running picks must start at zero
+  if (cudaMemsetAsync(ws, 0, mtp::kWsBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MTP_ERR_CUDA;
   return mtp_head_logits_argmax_batched(x, final_norm_w, lm_head, row_scale, w_dtype, logits, draft,
                                         status, ws, kStaticScratchBytes, B, H, V, eps, stream);

@@ -54,7 +54,6 @@ __device__ void argmax_finish(const ArgBest* best, int nb, ArgBest* wbest, const
       if (b < nb) wbest[warp * nb + b] = best[b];
   }
   __syncthreads();
-  ArgBest* part = reinterpret_cast<ArgBest*>(ws + kWsHeader);
   unsigned int* counter = reinterpret_cast<unsigned int*>(ws);
   if (threadIdx.x < nb) {
     ArgBest c{0.0f, -1};
@@ -62,7 +61,7 @@ __device__ void argmax_finish(const ArgBest* best, int nb, ArgBest* wbest, const
       const ArgBest o = wbest[w * nb + threadIdx.x];
       if (o.i >= 0) arg_update(c, o.v, o.i);
     }
-    part[blockIdx.x * nb + threadIdx.x] = c;
+    pick_publish(ws, threadIdx.x, c.v, c.i, a.index_base);
     __threadfence();
   }
   __syncthreads();
@@ -70,7 +69,7 @@ __device__ void argmax_finish(const ArgBest* best, int nb, ArgBest* wbest, const
   __syncthreads();
   if (is_last) {
     __threadfence();
-    combine_partials(part, gridDim.x, nb, a.draft, a.index_base, a.pick);
+    if (threadIdx.x < nb) pick_finish(ws, threadIdx.x, a.draft, a.pick);
     if (threadIdx.x == 0) {
       // every CTA has finished claiming rows: ready for the next launch
       atomicExch(reinterpret_cast<unsigned int*>(ws + kRowCounterOffset), 0u);
@@ -709,9 +708,7 @@ cudaError_t try_launch_regx(SweepArgs a, const DeviceInfo& di, unsigned grid, cu
 
 }  // namespace
 
-size_t sweep_workspace_bytes(int B) {
-  return static_cast<size_t>(kWsHeader) + static_cast<size_t>(kMaxGrid) * B * sizeof(ArgBest);
-}
+size_t sweep_workspace_bytes(int /*B*/) { return static_cast<size_t>(kWsBytes); }
 
 cudaError_t launch_sweep(const SweepArgs& in, cudaStream_t stream) {
   DeviceInfo di;

@@ -142,12 +142,10 @@ struct BFrags<MTP_W_FP8_E4M3, NT> {
   }
 };
 
-// CTA combine of per-warp bests (wbest[warp * kSeq + b]) and the last-CTA-done grid argmax
-// (scratch: kTcThreads entries of shared memory no longer in use).
-__device__ void tc_argmax_finish(int nb, const ArgBest* wbest, const SweepArgs& a, ArgBest* scratch) {
+// CTA combine of per-warp bests (wbest[warp * kSeq + b]) and the last-CTA-done grid argmax.
+__device__ void tc_argmax_finish(int nb, const ArgBest* wbest, const SweepArgs& a) {
   uint8_t* ws = a.ws;
   __shared__ int is_last;
-  ArgBest* part = reinterpret_cast<ArgBest*>(ws + kWsHeader);
   unsigned int* counter = reinterpret_cast<unsigned int*>(ws);
   if (threadIdx.x < nb) {
     ArgBest c{0.0f, -1};
@@ -155,7 +153,7 @@ __device__ void tc_argmax_finish(int nb, const ArgBest* wbest, const SweepArgs& 
       const ArgBest o = wbest[w * kSeq + threadIdx.x];
       if (o.i >= 0) arg_update(c, o.v, o.i);
     }
-    part[blockIdx.x * nb + threadIdx.x] = c;
+    pick_publish(ws, threadIdx.x, c.v, c.i, a.index_base);
     __threadfence();
   }
   __syncthreads();
@@ -163,7 +161,7 @@ __device__ void tc_argmax_finish(int nb, const ArgBest* wbest, const SweepArgs& 
   __syncthreads();
   if (is_last) {
     __threadfence();
-    combine_partials_coalesced(part, gridDim.x, nb, a.draft, a.index_base, a.pick, scratch);
+    if (threadIdx.x < nb) pick_finish(ws, threadIdx.x, a.draft, a.pick);
     if (threadIdx.x == 0) atomicExch(counter, 0u);
   }
 }
@@ -535,7 +533,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   __syncthreads();
   pdl_wait_prior_grid();  // the workspace may still be read by the kernel before (no-op if done)
-  tc_argmax_finish(B, wbest, a, reinterpret_cast<ArgBest*>(aring));  // the weight ring is idle now
+  tc_argmax_finish(B, wbest, a);
 }
 
 // ---------------------------------------------------------------------------- host side

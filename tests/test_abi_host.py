@@ -60,13 +60,14 @@ def test_strerror_covers_every_code(lib):
 
 
 def test_workspace_bytes(lib):
-    assert m.mtp_head_workspace_bytes(1, 6144, 154880) > 0
-    assert m.mtp_head_workspace_bytes(16, 6144, 154880) >= 16 * 8 * 152
     assert m.mtp_head_workspace_bytes(0, 6144, 154880) == 0
     assert m.mtp_head_workspace_bytes(17, 6144, 154880) == 0
     assert m.mtp_head_workspace_bytes(1, 0, 10) == 0
-    # the whole-step workspace also has room for the context-row input stage (the concat of the B rows, at least)
-    assert m.mtp_head_workspace_bytes(16, 6144, 154880) >= 128 + 8192 * 16 + 16 * 2 * 6144 * 2 + 16 * 4
+    # the output stage's part (2304 bytes whatever B), then room for the context-row input stage
+    for B in (1, 2, 7, 16):
+        for H in (64, 1000, 6144):
+            assert m.mtp_head_workspace_bytes(B, H, 154880) == 2304 + m.mtp_head_context_workspace_bytes(B, H)
+    assert m.mtp_head_workspace_bytes(16, 6144, 154880) >= 2304 + 16 * 2 * 6144 * 2 + 16 * 4  # concat, row flags
 
 
 def test_context_workspace_bytes(lib):
