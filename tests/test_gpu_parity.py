@@ -273,6 +273,42 @@ def test_planted_ties_lowest_index_wins(fp8):
     assert int(draft.item()) == min(planted)
 
 
+@pytest.mark.parametrize("B", [5, 16])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_batched_planted_ties_across_ctas(B, fp8):
+    """Each sequence gets its own four identical rows of lm_head (bit-identical largest logits)
+    spread over the vocabulary, so over different CTAs of the batched sweep: the lowest planted
+    row wins for every sequence, whatever order the CTAs' picks reach the workspace in; one
+    sequence with a NaN in x gives -1."""
+    H, V = 2048, 20000
+    c = Case(H, V, B, seed=31 + B)
+    x = synth._normal_bf16((B, H), 0.0, 1.0, torch.Generator().manual_seed(B), "cpu")
+    xhat = oracle.final_norm(_bits(x), c.wb["final_norm_w"], EPS)
+    rows = synth.pick_rows(V, 4 * B, seed=B).view(-1)
+    rows = rows[torch.randperm(4 * B, generator=torch.Generator().manual_seed(7))].view(B, 4)  # disjoint sets
+    W = c.w.lm_head
+    for b in range(B):
+        W = synth.plant_rows(W, rows[b], torch.from_numpy(oracle.bf16_to_f64(xhat[b])), 0.05)
+    Wd = W.to(DEV)
+    xg = x.to(DEV)
+    xg[B - 1, 100] = float("nan")
+    if fp8:
+        q = torch.empty((V, H), dtype=torch.uint8, device=DEV)
+        s = torch.empty(V, dtype=torch.float32, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        m.mtp_head_quantize_fp8(Wd, q, s, st)
+        logits, draft, status = c.output_gpu(xg, q, s, m.W_FP8_E4M3)
+    else:
+        logits, draft, status = c.output_gpu(xg, Wd, None, m.W_BF16)
+    assert status == 0
+    lg = logits.cpu()
+    for b in range(B - 1):
+        planted = rows[b].tolist()
+        assert len(set(lg[b, planted].view(torch.int32).tolist())) == 1  # bit-identical tie
+        assert int(draft[b]) == min(planted) == lowest_argmax(lg[b].double().numpy())
+    assert torch.isnan(lg[B - 1]).all() and int(draft[B - 1]) == -1
+
+
 def test_repeat_calls_are_bitwise_identical_and_graph_replay_matches():
     c = Case(2048, 30000, 2, seed=10)
     # x of the whole step (its input stage is the context-row GEMM here), eagerly
