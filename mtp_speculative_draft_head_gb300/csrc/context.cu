@@ -54,11 +54,15 @@ __global__ void __launch_bounds__(kCtxNormThreads) context_concat_rows_kernel(co
   __shared__ int ok_s;
   const int r = blockIdx.x;
   const int H = a.H;
-  pdl_wait_prior_grid();  // tokens and target_hidden may come from the preceding kernel
-  // The next kernel may start its independent work (weight streams) now; it waits for this
-  // grid's completion before it reads the concat. Every CTA of this grid has started by the
-  // time the next one launches, so it never holds SMs this grid still needs.
+  // The GEMM may launch at once, before this grid even waits for the kernel before it: its
+  // producer streams eh_proj (which depends on nothing) and waits for this grid's completion
+  // before it reads the concat. Launched this early, its CTAs take the SMs that the preceding
+  // kernel's CTAs leave as they finish, and its weight stream fills the HBM time that the end of
+  // that kernel leaves idle (a batched draft chain, after a sweep: 1.4 to 4 us a step, B = 2..16).
+  // Every CTA of this grid has started by the time the GEMM launches, so the GEMM never holds
+  // SMs this grid still needs.
   pdl_launch_dependents();
+  pdl_wait_prior_grid();  // tokens and target_hidden may come from the preceding kernel
   if (threadIdx.x == 0) {
     const int32_t tok = a.tokens[r];
     const int ok = (tok >= 0 && tok < a.V) ? 1 : 0;
