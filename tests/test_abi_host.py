@@ -136,6 +136,8 @@ def test_input_stage_validation(lib, kw, code):
     (dict(ws=A + 8), m.ERR_ALIGN),
     (dict(ws=None), m.ERR_WORKSPACE),
     (dict(ws_bytes=16), m.ERR_WORKSPACE),
+    (dict(ws_bytes=2303), m.ERR_WORKSPACE),            # one byte short of the output stage's part
+    (dict(ws_bytes=2303, B=16), m.ERR_WORKSPACE),      # ... which is the same for every B
 ])
 def test_output_stage_validation(lib, kw, code):
     assert _output(lib, **kw) == code

@@ -309,6 +309,29 @@ def test_batched_planted_ties_across_ctas(B, fp8):
     assert torch.isnan(lg[B - 1]).all() and int(draft[B - 1]) == -1
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_output_stage_in_its_smallest_workspace(fp8):
+    """The output stage needs the same 2304 bytes of workspace for any B: a 16-sequence sweep in
+    exactly that much (zero-filled once) gives the bits of a sweep in a whole-step workspace, twice
+    in a row (the counters and the running picks are back to zero after each call)."""
+    c = Case(1000, 5003, 16, seed=41)
+    x = synth._normal_bf16((16, c.H), 0.0, 1.0, torch.Generator().manual_seed(41), "cpu").to(DEV)
+    if fp8:
+        q, s_, _ = c.quantize_gpu()
+        W, scale, wt = q, s_, m.W_FP8_E4M3
+    else:
+        W, scale, wt = c.g["lm_head"], None, m.W_BF16
+    ref_lg, ref_d, st = c.output_gpu(x, W, scale, wt)
+    assert st == 0
+    small = torch.zeros(2304, dtype=torch.uint8, device=DEV)
+    for _ in range(2):
+        lg = torch.empty((16, c.V), dtype=torch.float32, device=DEV)
+        d = torch.empty(16, dtype=torch.int32, device=DEV)
+        m.mtp_head_logits_argmax_batched(x, c.g["final_norm_w"], W, scale, wt, lg, d, small, None, EPS)
+        torch.cuda.synchronize()
+        assert torch.equal(lg.view(torch.int32), ref_lg.view(torch.int32)) and torch.equal(d, ref_d)
+
+
 def test_repeat_calls_are_bitwise_identical_and_graph_replay_matches():
     c = Case(2048, 30000, 2, seed=10)
     # x of the whole step (its input stage is the context-row GEMM here), eagerly
