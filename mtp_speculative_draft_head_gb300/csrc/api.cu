@@ -13,6 +13,7 @@
 #include "../../include/mtp_head.h"
 #include "common.cuh"
 #include "internal.h"
+#include "host_back.h"
 
 namespace {
 
@@ -136,10 +137,10 @@ int run_step_input(const uint16_t* embed, const uint16_t* enorm_w, const uint16_
 }
 
 // index_base / pick: a vocabulary shard's first global row and its exchange keys (may be null).
-int run_output(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_head,
-               const float* row_scale, int w_dtype, float* logits, int32_t* draft, int32_t* status,
-               void* workspace, int B, int H, int V, float eps, void* stream, int32_t index_base = 0,
-               int64_t* pick = nullptr) {
+mtp::SweepArgs output_args(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_head,
+                           const float* row_scale, int w_dtype, float* logits, int32_t* draft, int32_t* status,
+                           void* workspace, int B, int H, int V, float eps, int32_t index_base = 0,
+                           int64_t* pick = nullptr) {
   mtp::SweepArgs a{};
   a.index_base = index_base;
   a.pick = pick;
@@ -158,6 +159,15 @@ int run_output(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_h
   a.eps = eps;
   a.inv_h = 1.0 / static_cast<double>(H);
   a.wait_ns = mtp::stage_wait_ns();
+  return a;
+}
+
+int run_output(const uint16_t* x, const uint16_t* final_norm_w, const void* lm_head,
+               const float* row_scale, int w_dtype, float* logits, int32_t* draft, int32_t* status,
+               void* workspace, int B, int H, int V, float eps, void* stream, int32_t index_base = 0,
+               int64_t* pick = nullptr) {
+  const mtp::SweepArgs a = output_args(x, final_norm_w, lm_head, row_scale, w_dtype, logits, draft, status,
+                                       workspace, B, H, V, eps, index_base, pick);
   return map_cuda(mtp::launch_sweep(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -287,10 +297,20 @@ std::shared_ptr<StepGraph> record_step(const HostStep& s, int device) {
       v = run_step_input(s.embed, s.enorm_w, s.hnorm_w, s.eh_proj, s.tokens_dev, s.hidden_dev, s.x_dev, s.status,
                          s.B, s.H, s.V, s.eps, s.stream, cat);
     }
-    if (v == MTP_OK)
+    // one sequence: the sweep's last CTA writes the draft, the status and the completion word
+    // itself; otherwise a small kernel after the sweep does
+    bool handed = false;
+    if (v == MTP_OK) {
+      const mtp::HostBack hb{reinterpret_cast<int32_t*>(dbase + tok_bytes), reinterpret_cast<uint32_t*>(dbase + 2 * tok_bytes)};
+      v = map_cuda(mtp::launch_sweep_handback(output_args(s.x_dev, s.final_norm_w, s.lm_head, s.row_scale, s.w_dtype,
+                                                          nullptr, s.draft_dev, s.status, s.workspace, s.B, s.H,
+                                                          s.V, s.eps),
+                                              hb, s.stream, &handed));
+    }
+    if (v == MTP_OK && !handed)
       v = run_output(s.x_dev, s.final_norm_w, s.lm_head, s.row_scale, s.w_dtype, nullptr, s.draft_dev, s.status,
                      s.workspace, s.B, s.H, s.V, s.eps, s.stream);
-    if (v == MTP_OK)
+    if (v == MTP_OK && !handed)
       v = map_cuda(mtp::launch_host_out(s.draft_dev, reinterpret_cast<int32_t*>(dbase + tok_bytes), s.status,
                                         reinterpret_cast<int32_t*>(dbase + 2 * tok_bytes), s.B,
                                         reinterpret_cast<const uint32_t*>(dbase + 2 * tok_bytes + 8),

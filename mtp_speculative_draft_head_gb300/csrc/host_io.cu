@@ -1,6 +1,7 @@
 // Host <-> device moves of the host-buffer draft step as kernels, for its recorded CUDA graph:
 // the inputs are read straight from mapped pinned host memory (zero copy) and the draft written
-// straight back. Against the three copy operations they replace (~13 us of GPU time a step),
+// straight back (for one sequence by the sweep's last CTA itself, host_back.h; otherwise by
+// host_out_kernel after the sweep). Against the three copy operations they replace (~13 us of GPU time a step),
 // they need no copy engine, and with programmatic dependent launch the input stage starts its
 // weight stream while the first one runs and the last one is waiting for the sweep.
 // Plain loads and stores only: a host-mapped address is a valid global address for them.

@@ -33,6 +33,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "host_back.h"
 
 namespace mtp {
 
@@ -42,8 +43,11 @@ namespace {
 // Per-CTA epilogue: combine warp bests, publish the CTA partial, and let the last CTA finish.
 // best[] is uniform across the lanes of a warp.
 // ------------------------------------------------------------------------------------------
+// hb (a recorded host-buffer step, else null): the last CTA also hands the drafts and the status
+// back to mapped host memory, then sets the completion word the host polls.
 template <int NB>
-__device__ void argmax_finish(const ArgBest* best, int nb, ArgBest* wbest, const SweepArgs& a) {
+__device__ void argmax_finish(const ArgBest* best, int nb, ArgBest* wbest, const SweepArgs& a,
+                              const HostBack* hb = nullptr) {
   uint8_t* ws = a.ws;
   __shared__ int is_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -70,6 +74,19 @@ __device__ void argmax_finish(const ArgBest* best, int nb, ArgBest* wbest, const
   if (is_last) {
     __threadfence();
     if (threadIdx.x < nb) pick_finish(ws, threadIdx.x, a.draft, a.pick);
+    if (hb != nullptr) {
+      if (static_cast<int>(threadIdx.x) < nb) {
+        hb->draft[threadIdx.x] = a.draft[threadIdx.x];  // written by this thread just above
+        __threadfence_system();
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        volatile uint32_t* w = hb->words;
+        if (a.status != nullptr) w[0] = static_cast<uint32_t>(*reinterpret_cast<const volatile int32_t*>(a.status));
+        __threadfence_system();
+        w[3] = w[2];
+      }
+    }
     if (threadIdx.x == 0) {
       // every CTA has finished claiming rows: ready for the next launch
       atomicExch(reinterpret_cast<unsigned int*>(ws + kRowCounterOffset), 0u);
@@ -240,7 +257,7 @@ __device__ void final_norm_prologue(const SweepArgs& a, int nb, uint16_t* vec, i
 constexpr int kGroup = 8;
 
 template <int WT, int NVL, int NWR, bool kMixed, bool kCvt>
-__global__ void __launch_bounds__(NWR * 32, 1) sweep_regx_kernel(const SweepArgs a) {
+__device__ __forceinline__ void sweep_regx_body(const SweepArgs& a, const HostBack* hb) {
   constexpr int EB = (WT == MTP_W_BF16) ? 2 : 1;
   constexpr int EPV = 16 / EB;
   constexpr int H = NVL * 32 * EPV;
@@ -453,7 +470,18 @@ __global__ void __launch_bounds__(NWR * 32, 1) sweep_regx_kernel(const SweepArgs
   }
   __syncwarp();
   best = warp_arg_reduce(best);
-  argmax_finish<1>(&best, 1, wbest, a);
+  argmax_finish<1>(&best, 1, wbest, a, hb);
+}
+
+template <int WT, int NVL, int NWR, bool kMixed, bool kCvt>
+__global__ void __launch_bounds__(NWR * 32, 1) sweep_regx_kernel(const SweepArgs a) {
+  sweep_regx_body<WT, NVL, NWR, kMixed, kCvt>(a, nullptr);
+}
+
+// The same for a recorded host-buffer step (HostBack).
+template <int WT, int NVL, int NWR, bool kMixed, bool kCvt>
+__global__ void __launch_bounds__(NWR * 32, 1) sweep_regx_hb_kernel(const SweepArgs a, const HostBack hb) {
+  sweep_regx_body<WT, NVL, NWR, kMixed, kCvt>(a, &hb);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -668,10 +696,11 @@ cudaError_t launch_tma(SweepArgs a, const DeviceInfo& di, unsigned grid, size_t 
 #define MTP_FP8_CVT 1
 #endif
 
-// B = 1 register-xhat kernel, if this H has an instantiation and the stages fit.
+// B = 1 register-xhat kernel, if this H has an instantiation and the stages fit; with hb, the
+// kernel that also hands the result back to host memory.
 template <int WT>
 cudaError_t try_launch_regx(SweepArgs a, const DeviceInfo& di, unsigned grid, cudaStream_t stream,
-                            bool* launched) {
+                            bool* launched, const HostBack* hb = nullptr) {
   constexpr int EB = (WT == MTP_W_BF16) ? 2 : 1;
   constexpr int EPV = 16 / EB;
   constexpr int NWR = (WT == MTP_W_BF16) ? MTP_REGX_WARPS_BF16 : MTP_REGX_WARPS_FP8;
@@ -680,18 +709,37 @@ cudaError_t try_launch_regx(SweepArgs a, const DeviceInfo& di, unsigned grid, cu
   if (!MTP_REGX || a.H % (32 * EPV) != 0) return cudaSuccess;
   const int nvl = a.H / (32 * EPV);
   void (*k)(SweepArgs) = nullptr;
+  void (*khb)(SweepArgs, HostBack) = nullptr;
   if constexpr (WT == MTP_W_BF16) {
     switch (nvl) {
-      case 16: k = sweep_regx_kernel<WT, 16, NWR, kMixedDefault, kCvt>; break;  // H = 4096
-      case 24: k = sweep_regx_kernel<WT, 24, NWR, kMixedDefault, kCvt>; break;  // H = 6144
-      case 28: k = sweep_regx_kernel<WT, 28, NWR, kMixedDefault, kCvt>; break;  // H = 7168
+      case 16:  // H = 4096
+        k = sweep_regx_kernel<WT, 16, NWR, kMixedDefault, kCvt>;
+        khb = sweep_regx_hb_kernel<WT, 16, NWR, kMixedDefault, kCvt>;
+        break;
+      case 24:  // H = 6144
+        k = sweep_regx_kernel<WT, 24, NWR, kMixedDefault, kCvt>;
+        khb = sweep_regx_hb_kernel<WT, 24, NWR, kMixedDefault, kCvt>;
+        break;
+      case 28:  // H = 7168
+        k = sweep_regx_kernel<WT, 28, NWR, kMixedDefault, kCvt>;
+        khb = sweep_regx_hb_kernel<WT, 28, NWR, kMixedDefault, kCvt>;
+        break;
       default: return cudaSuccess;
     }
   } else {
     switch (nvl) {
-      case 8: k = sweep_regx_kernel<WT, 8, NWR, kMixedDefault, kCvt>; break;    // H = 4096
-      case 12: k = sweep_regx_kernel<WT, 12, NWR, kMixedDefault, kCvt>; break;  // H = 6144
-      case 14: k = sweep_regx_kernel<WT, 14, NWR, kMixedDefault, kCvt>; break;  // H = 7168
+      case 8:  // H = 4096
+        k = sweep_regx_kernel<WT, 8, NWR, kMixedDefault, kCvt>;
+        khb = sweep_regx_hb_kernel<WT, 8, NWR, kMixedDefault, kCvt>;
+        break;
+      case 12:  // H = 6144
+        k = sweep_regx_kernel<WT, 12, NWR, kMixedDefault, kCvt>;
+        khb = sweep_regx_hb_kernel<WT, 12, NWR, kMixedDefault, kCvt>;
+        break;
+      case 14:  // H = 7168
+        k = sweep_regx_kernel<WT, 14, NWR, kMixedDefault, kCvt>;
+        khb = sweep_regx_hb_kernel<WT, 14, NWR, kMixedDefault, kCvt>;
+        break;
       default: return cudaSuccess;
     }
   }
@@ -703,12 +751,33 @@ cudaError_t try_launch_regx(SweepArgs a, const DeviceInfo& di, unsigned grid, cu
   if (S > kMaxStages) S = kMaxStages;
   a.stages = S;
   *launched = true;
+  if (hb != nullptr) {
+    HostBack h = *hb;
+    void* args[] = {&a, &h};
+    return launch_pdl(reinterpret_cast<const void*>(khb), dim3(grid), dim3(NWR * 32), fixed + S * per_stage, stream,
+                      args);
+  }
   return launch_sweep_kernel(k, grid, NWR * 32, fixed + S * per_stage, stream, a);
 }
 
 }  // namespace
 
 size_t sweep_workspace_bytes(int /*B*/) { return static_cast<size_t>(kWsBytes); }
+
+cudaError_t launch_sweep_handback(const SweepArgs& in, const HostBack& hb, cudaStream_t stream, bool* done) {
+  *done = false;
+  DeviceInfo di;
+  cudaError_t err = device_info(&di);
+  if (err != cudaSuccess) return err;
+  const int EB = (in.w_dtype == MTP_W_BF16) ? 2 : 1;
+  if (in.B != 1 || (static_cast<int64_t>(in.H) * EB) % 16 != 0) return cudaSuccess;
+  const int64_t want = (static_cast<int64_t>(in.V) + kWarps - 1) / kWarps;
+  int64_t g = di.sm_count < want ? di.sm_count : want;
+  if (g > kMaxGrid) g = kMaxGrid;
+  if (g < 1) g = 1;
+  return in.w_dtype == MTP_W_BF16 ? try_launch_regx<MTP_W_BF16>(in, di, static_cast<unsigned>(g), stream, done, &hb)
+                                  : try_launch_regx<MTP_W_FP8_E4M3>(in, di, static_cast<unsigned>(g), stream, done, &hb);
+}
 
 cudaError_t launch_sweep(const SweepArgs& in, cudaStream_t stream) {
   DeviceInfo di;
