@@ -618,7 +618,10 @@ def test_whole_step_input_without_the_gemm_shape(H, B):
     assert torch.equal(x_fw.view(torch.int16), x_in.view(torch.int16))
 
 
-@pytest.mark.parametrize("H,B", [(256, 3), (100, 1)])  # moves as kernels; B * H % 8 != 0: copy operations
+# (256, 3): moves as kernels, the small kernel after the sweep hands the drafts back; (4096, 1):
+# the register-resident sweep's last CTA hands the draft and the status back itself; (100, 1):
+# B * H % 8 != 0, copy operations
+@pytest.mark.parametrize("H,B", [(256, 3), (4096, 1), (100, 1)])
 @pytest.mark.parametrize("fp8", [False, True])
 def test_host_forward_graph_replays_match_device_path(fp8, H, B):
     """On a non-default stream the host-buffer step runs directly on the first call, then replays
